@@ -1,0 +1,363 @@
+#!/usr/bin/env python
+"""Benchmark of the joint audio-video attention sub-block forward on GB300.
+
+One step = one fused sub-block forward (modulate -> QKV projection + 3D RoPE
+-> joint attention -> output projection + gated residual) over the full-size
+packed sequence: L = 58,758 tokens (358 text + 57,600 video + 800 audio),
+d = 5120, 40 heads x 128, full attention, batch 1.  Reports block TFLOP/s
+(algorithmic FLOPs 6Ld^2 + 4L^2d + 2Ld^2 over device time), tokens/s, the
+attention kernel against the bf16 tensor roofline, an end-to-end number
+through the public API with host buffers, and the CPU fp64 oracle timed on a
+bounded sample of the same workload.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Under torchrun each rank runs an independent replica (the block does not
+shard: replicas only); the printed value is the aggregate over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attn-block fwd TFLOP/s & tokens/s at L=58,758; % of GB300 dense BF16 peak"
+UNIT = "TFLOP/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return FALLBACK_PEAKS, "fallback"
+
+
+# ---------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------- oracle sample
+def oracle_sample(cfg, inp, scale_factor: float = 1.0):
+    """Time the CPU fp64 oracle on a bounded sample of the block workload.
+
+    Stages and sample sizes: modulate on R1 rows, QKV projection + RoPE on R2
+    rows, attention for R3 query rows of H3 heads against all L keys (random
+    workload-shaped qkv), output projection + gated residual on R2 rows.
+    Each stage's time is scaled to the full block by its work ratio.
+    Returns (extrapolated full-block seconds, sample description, cores).
+    """
+    import numpy as np
+    import oracle as orc
+    from h3inputs import attention_qkv
+
+    L, d, H = cfg.L, cfg.d, cfg.n_heads
+    R1 = int(4096 * scale_factor)
+    R2 = int(384 * scale_factor)
+    R3, H3 = int(128 * scale_factor), 4
+    f64 = lambda t: t.float().double().numpy()
+    mod, pos = orc.packed_layout(cfg.n_text, cfg.video_t, cfg.video_h, cfg.video_w,
+                                 cfg.audio_channels, cfg.audio_steps)
+    rows1 = np.linspace(0, L - 1, R1).astype(np.int64)
+    rows2 = np.linspace(0, L - 1, R2).astype(np.int64)
+    x1, x2 = f64(inp["x"][rows1]), f64(inp["x"][rows2])
+    shift, scale, gate = f64(inp["shift"]), f64(inp["scale"]), f64(inp["gate"])
+    wqkv, wo = f64(inp["Wqkv"]), f64(inp["Wo"])
+    qkv_s = f64(attention_qkv(L, H3, seed=99))
+    rows3 = np.linspace(0, L - 1, R3).astype(np.int64)
+
+    t = time.perf_counter()
+    orc.adaln_modulate(x1, mod[rows1], shift, scale, cfg.ln_eps)
+    t_mod = time.perf_counter() - t
+    t = time.perf_counter()
+    y2 = orc.adaln_modulate(x2, mod[rows2], shift, scale, cfg.ln_eps)
+    q = orc.mrope(orc.linear(y2, wqkv), pos[rows2], H)
+    t_qkv = time.perf_counter() - t
+    t = time.perf_counter()
+    o, _ = orc.attention(qkv_s, H3, 128, rows=rows3)
+    t_att = time.perf_counter() - t
+    t = time.perf_counter()
+    orc.gated_residual(x2, orc.linear(q[:, :d], wo), mod[rows2], gate)
+    t_out = time.perf_counter() - t
+    full = (t_mod * L / R1 + t_qkv * L / R2 + t_att * (L / R3) * (H / H3) + t_out * L / R2)
+    sample = (f"oracle (numpy fp64) on {R1} rows of modulate, {R2} rows of QKV projection + "
+              f"RoPE and of output projection + gated residual, {R3} query rows x {H3} heads "
+              f"of attention over all {L} keys; scaled to the full block by work ratio "
+              f"(sample {t_mod + t_qkv + t_att + t_out:.1f} s)")
+    cores = len(os.sched_getaffinity(0))
+    return full, sample, cores, t_mod + t_qkv + t_att + t_out
+
+
+# ---------------------------------------------------------------------------- reference arm
+def run_reference(args, cfg):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    from h3inputs import block_inputs
+    inp = block_inputs(cfg)
+    flops = cfg.flops()
+    times, sample_s = [], []
+    for i in range(args.warmup + args.steps):
+        full, sample, cores, s = oracle_sample(cfg, inp, scale_factor=2.0)
+        if i >= args.warmup:
+            times.append(full)
+            sample_s.append(s)
+    full = statistics.mean(times)
+    value = flops / full / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": full * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "joint A/V DiT attention sub-block, L=58758 (358 text + "
+                               "57600 video + 800 audio), d=5120, 40x128 heads, full attention",
+                   "L": cfg.L, "d": cfg.d, "heads": cfg.n_heads},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "tokens_per_s": cfg.L / full,
+        "note": "each step is a bounded oracle sample; ms_per_step is the extrapolated "
+                "full-block CPU time",
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------- GPU arm
+def run_gpu(args, cfg):
+    import torch
+    import torch.distributed as dist
+    import joint_audio_video_gb300 as h3
+    from joint_audio_video_gb300 import build as h3build
+    from h3inputs import block_inputs
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    if rank == 0 or world == 1:
+        h3build.build()
+    if world > 1:
+        dist.barrier()
+    h3.load()
+    dev = torch.device("cuda", local)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    L, d, H = cfg.L, cfg.d, cfg.n_heads
+    inp = block_inputs(cfg)
+    mod, pos = h3.h3_build_packed_layout(cfg.n_text, cfg.video_t, cfg.video_h, cfg.video_w,
+                                         cfg.audio_channels, cfg.audio_steps)
+    x = inp["x"].to(dev)
+    wqkv, wo = inp["Wqkv"].to(dev), inp["Wo"].to(dev)
+    shift, scale, gate = inp["shift"].to(dev), inp["scale"].to(dev), inp["gate"].to(dev)
+    mod_d, pos_d = torch.from_numpy(mod).to(dev), torch.from_numpy(pos).to(dev)
+    desc = h3.BlockDesc.make(L=L, d=d, n_heads=H, rope_sec=cfg.rope_sections,
+                             rope_base=cfg.rope_base, ln_eps=cfg.ln_eps, n_mod=cfg.n_mod)
+    nbytes = h3.h3_workspace_size(desc)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    out = torch.empty(L, d, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(events=None):
+        h3.h3_attn_block_fwd_profiled(desc, x, mod_d, pos_d, shift, scale, gate, wqkv, wo, ws,
+                                      nbytes, out, events, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    st = h3.h3_sync_status(stream)
+    if st != 0:
+        raise RuntimeError(f"device status after warm-up: {h3.h3_status_string(st)}")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    barrier()
+    torch.cuda.synchronize(dev)
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    wall0 = time.perf_counter()
+    t0.record(stream)
+    for k in range(args.steps):
+        step(evs[k])
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - wall0
+    barrier()
+    clocks = sampler.stop() if sampler else None
+    st = h3.h3_sync_status(stream)
+    if st != 0:
+        raise RuntimeError(f"device status after timed steps: {h3.h3_status_string(st)}")
+    ms = t0.elapsed_time(t1) / args.steps
+    names = ["modulate", "qkv_rope_gemm", "attention", "out_gemm"]
+    per = {n: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in evs)
+           for i, n in enumerate(names)}
+    if world > 1:
+        tt = torch.tensor([ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+
+    # ---- end to end through the public API with host buffers
+    x_host = inp["x"].pin_memory()
+    mod_host = {k: inp[k].pin_memory() for k in ("shift", "scale", "gate")}
+    out_host = torch.empty(L, d, dtype=torch.bfloat16).pin_memory()
+    h2d = x_host.numel() * 2 + sum(v.numel() * 4 for v in mod_host.values())
+    d2h = out_host.numel() * 2
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def e2e_step():
+        x.copy_(x_host, non_blocking=True)
+        shift.copy_(mod_host["shift"], non_blocking=True)
+        scale.copy_(mod_host["scale"], non_blocking=True)
+        gate.copy_(mod_host["gate"], non_blocking=True)
+        h3.h3_attn_block_fwd(desc, x, mod_d, pos_d, shift, scale, gate, wqkv, wo, ws, nbytes,
+                             out, stream=stream)
+        out_host.copy_(out, non_blocking=True)
+
+    for _ in range(max(1, min(args.warmup, 2))):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier()
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    if world > 1:
+        tt = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+    st = h3.h3_sync_status(stream)
+    if st != 0:
+        raise RuntimeError(f"device status after e2e steps: {h3.h3_status_string(st)}")
+
+    flops = cfg.flops()
+    value = world * flops / (ms * 1e-3) / 1e12
+    attn_flops = 4.0 * L * L * d
+    peaks, peak_kind = _peaks()
+    peak = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
+    achieved = attn_flops / (per["attention"] * 1e-3) / 1e12
+    traffic = None
+    tf = os.path.join(ROOT, "profiles", "attention_traffic.json")
+    if os.path.exists(tf):
+        with open(tf) as f:
+            traffic = json.load(f).get("bytes_per_launch_full")
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": "joint A/V DiT attention sub-block, L=58758 (358 text + 57600 "
+                               "video + 800 audio), d=5120, 40x128 heads, full attention, "
+                               "batch 1",
+                   "L": L, "d": d, "heads": H, "causal": False,
+                   "l2": "inputs larger than L2 (x 602 MB, qkv 1.8 GB per step)",
+                   "parallelism": f"replicas x{world}"},
+        "tokens_per_s": world * L / (ms * 1e-3),
+        "pct_of_bf16_peak_block": flops / (ms * 1e-3) / 1e12 / peak,
+        "kernel_ms": per,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "kernel": "attention (attn_fwd_kernel)",
+                     "peak_kind": f"{peak_kind} bf16 sustained (kernel inside a long step)"},
+        "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": 4 * args.steps,
+        "clocks": clocks,
+        "wall_s_timed": wall,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        full, sample, cores, _ = oracle_sample(cfg, inp, scale_factor=8.0)
+        line["cpu_baseline"] = {"value": flops / full / 1e12, "unit": UNIT, "cores": cores,
+                                "kind": "oracle", "sample": sample,
+                                "extrapolated_block_s": full}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__,
+                                 formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="h3", choices=["h3", "reference"])
+    ap.add_argument("--config", default="full", help="block workload (default: full, L=58758)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)        # at least 3 untimed warm-up steps
+    from h3inputs import CONFIGS
+    cfg = CONFIGS[args.config]
+    if args.impl == "reference":
+        return run_reference(args, cfg)
+    return run_gpu(args, cfg)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

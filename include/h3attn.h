@@ -1,0 +1,219 @@
+/*
+ * h3attn — C ABI of the GB300 (sm_103a) joint audio-video attention sub-block.
+ *
+ * One attention sub-block of a single-stream joint audio-video Diffusion
+ * Transformer of the MiniMax-H3 kind, run over one packed sequence of text,
+ * video and audio tokens:
+ *
+ *   y   = LN(x) * (1 + scale[mod]) + shift[mod]          h3_adaln_modulate
+ *   qkv = y Wqkv^T                                        h3_qkv_proj
+ *   Q,K <- 3D (t,h,w) rotary embedding                    h3_mrope_apply
+ *   O   = softmax(Q K^T / sqrt(dh) [+ causal]) V          h3_joint_attn_fwd
+ *   out = x + gate[mod] * (O Wo^T)                        h3_out_proj_gated_residual
+ *   all of the above in one call                          h3_attn_block_fwd
+ *
+ * Sources (web pages):
+ *   [H3-RL] "DiffusionNFT on MiniMax H3: Open-Source RL Training for Joint
+ *           Audio-Video Generation", section "MiniMax H3 and Why Joint
+ *           Audio-Video Generation Complicates RL Training" (3D multimodal RoPE
+ *           over time/height/width; modality-specific AdaLN branches whose
+ *           outputs are cacheable) and section "How VeRL-Omni's Adapter
+ *           Architecture Keeps H3-Specific Logic Contained" (to_q, to_k, to_v,
+ *           to_out.0 projections, fused in the rollout network).
+ *   [VeRL]  "多模态强化学习工程解析：VeRL-Omni 架构与 MiniMax-H3 训练实录",
+ *           三 目标模型 (shared attention weights and AdaLN modulation across
+ *           modalities; causal attention mentioned) and 5.2 LoRA 权重切分不一致
+ *           (Q, K, V packed into one matrix for inference).
+ *   [vLLM]  "Joint Audio-Video Generation in Production: Architecture Deep Dive
+ *           into MiniMax-H3 and vLLM-Omni", §1 Unified Architecture (one shared
+ *           attention context over 58,758 tokens, 50 denoising steps), §3 Packed
+ *           Sequences and Modality Identity Preservation (tags, positions),
+ *           §6 Boundary Trimming for Packed Attention (only the effective
+ *           tokens may enter the kernel).
+ *
+ * Conventions common to every call
+ *   - bf16 tensors are passed as uint16_t bit patterns; fp32 as float.
+ *   - Matrices are row-major; a row is one token.  Weights use the
+ *     nn.Linear layout W[out_features][in_features].
+ *   - Every device pointer must be 16-byte aligned and non-NULL (except an
+ *     optional output documented as such).  The caller owns every buffer;
+ *     no call allocates device memory.
+ *   - Every device call is asynchronous on the caller's stream.  Argument
+ *     errors are detected on the host before anything is launched.
+ *   - L is the exact token count (>= 1); nothing is padded and no token past
+ *     L is read as a key (the pages' boundary-trim requirement).
+ *   - d % 128 == 0, 128 <= d <= 16384; head_dim must be 128; 1 <= n_mod <= 255.
+ *   - A kernel that finds an out-of-range modality id or gives up on a
+ *     bounded wait records it in a per-device status word; h3_sync_status()
+ *     reports and clears it.  No C++ exception crosses this boundary.
+ */
+#ifndef H3ATTN_H_
+#define H3ATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int h3_status;
+#define H3_OK 0
+#define H3_ERR_INVALID_ARG 1   /* bad pointer, size or alignment; nothing launched */
+#define H3_ERR_UNSUPPORTED 2   /* valid but not implemented (e.g. head_dim != 128) */
+#define H3_ERR_CUDA 3          /* a CUDA runtime call or launch failed */
+#define H3_ERR_TIMEOUT 4       /* a kernel gave up on a bounded wait (device status) */
+#define H3_ERR_BAD_INDEX 5     /* a modality id >= n_mod was met (device status) */
+#define H3_ERR_WORKSPACE 6     /* workspace smaller than h3_workspace_size() */
+
+/* Same handle as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st* h3_stream_t;
+
+/* Shape and options of one sub-block. */
+typedef struct {
+  int32_t L;            /* tokens in the packed sequence, >= 1 */
+  int32_t d;            /* hidden size = n_heads * head_dim */
+  int32_t n_heads;
+  int32_t head_dim;     /* must be 128 */
+  int32_t rope_sec[3];  /* rotary dims of the t, h, w axes; even, summing to head_dim */
+  float rope_base;      /* frequency base (> 1), e.g. 10000 */
+  float ln_eps;         /* LayerNorm epsilon (>= 0), e.g. 1e-6 */
+  int32_t causal;       /* 0: full bidirectional attention; 1: key index <= query index */
+  int32_t n_mod;        /* number of modalities (rows of shift/scale/gate) */
+} h3_block_desc;
+
+/* Text for a status code (static storage). */
+const char* h3_status_string(h3_status s);
+
+/* Library version, e.g. "h3attn 0.1.0 sm_103a". */
+const char* h3_version(void);
+
+/*
+ * Packed layout metadata (host, integer; [vLLM] §3 data-flow table: row type,
+ * position indices, modality tags).  Token order: text [0, T), video
+ * row-major over (t, h, w), audio channel-major (token T + V + c*S + s).
+ * mod: 0 text, 1 video, 2 audio.  pos[n] = (t, h, w): text (i, i, i), video
+ * (t, h, w), audio (step, 0, channel), zero-based per modality.
+ *   mod [capacity] uint8, pos [capacity][3] int32: host buffers owned by the caller.
+ * Writes L = T + t*h*w + channels*steps tokens; returns H3_ERR_INVALID_ARG if a
+ * count is negative, L == 0, L > capacity or L > INT32_MAX.
+ */
+h3_status h3_build_packed_layout(int32_t n_text, int32_t video_t, int32_t video_h,
+                                 int32_t video_w, int32_t audio_channels, int32_t audio_steps,
+                                 uint8_t* mod, int32_t* pos, int64_t capacity);
+
+/*
+ * Modality-indexed AdaLN LayerNorm + modulate ([H3-RL] AdaLN branches;
+ * [VeRL] 三):  y[n] = (x[n] - mean) / sqrt(biased var + eps) * (1 + scale[m])
+ * + shift[m], m = mod[n]; statistics in fp32.
+ *   x [L][d] bf16, mod [L] uint8, shift/scale [n_mod][d] fp32 -> y [L][d] bf16.
+ * A row whose modality id is >= n_mod is written as NaN and flags H3_ERR_BAD_INDEX.
+ */
+h3_status h3_adaln_modulate(const uint16_t* x, const uint8_t* mod, const float* shift,
+                            const float* scale, int32_t L, int32_t d, int32_t n_mod, float eps,
+                            uint16_t* y, h3_stream_t stream);
+
+/*
+ * Fused QKV projection ([VeRL] 5.2: Q, K, V packed in one matrix):
+ *   qkv[n] = y[n] Wqkv^T, no bias; fp32 accumulation on the tensor cores.
+ *   y [L][d] bf16, Wqkv [3d][d] bf16 -> qkv [L][3d] bf16, columns [Q | K | V],
+ *   head h at columns h*128 .. h*128+127 inside each block.  Q and K are NOT
+ *   rotated (see h3_mrope_apply).  qkv must not alias y.
+ */
+h3_status h3_qkv_proj(const uint16_t* y, const uint16_t* Wqkv, int32_t L, int32_t d,
+                      uint16_t* qkv, h3_stream_t stream);
+
+/*
+ * 3D multimodal rotary embedding over (t, h, w) ([H3-RL]; [vLLM] §3), in place
+ * on the Q and K blocks of qkv [L][3*H*dh]; V is untouched.  Head dims
+ * [0, s0) follow t, [s0, s0+s1) follow h, the rest w.  Inside a section of
+ * n_a dims, pair (2j, 2j+1) turns by pos[n][a] * base^(-2j/n_a):
+ *   (u, v) -> (u cos - v sin, u sin + v cos); fp32 math, bf16 storage.
+ *   pos [L][3] int32 (t, h, w).
+ */
+h3_status h3_mrope_apply(uint16_t* qkv, const int32_t* pos, int32_t L, int32_t n_heads,
+                         int32_t head_dim, const int32_t sec[3], float base, h3_stream_t stream);
+
+/*
+ * Joint attention over the whole packed sequence ([vLLM] §1 shared attention
+ * context; §6 only the L effective tokens take part; [VeRL] 三 causal option):
+ *   O[n, h] = sum_j softmax_j(q_n . k_j * sm_scale) v_j over keys j in [0, L)
+ *   (j <= n when causal).  bf16 tensor-core products, fp32 softmax/accumulation.
+ *   qkv [L][3*H*dh] bf16 (Q, K rotated) -> O [L][H*dh] bf16.
+ *   lse: optional [H][L] fp32 natural-log sum of exp(scores*sm_scale), or NULL.
+ *   sm_scale > 0 (1/sqrt(head_dim) for the block).  O must not alias qkv.
+ */
+h3_status h3_joint_attn_fwd(const uint16_t* qkv, int32_t L, int32_t n_heads, int32_t head_dim,
+                            int32_t causal, float sm_scale, uint16_t* O, float* lse,
+                            h3_stream_t stream);
+
+/*
+ * Output projection + per-modality gated residual ([H3-RL] to_out.0 and the
+ * AdaLN gate):  out[n] = x_res[n] + gate[mod[n]] * (O[n] Wo^T); fp32 epilogue.
+ *   O [L][d] bf16, Wo [d][d] bf16, x_res [L][d] bf16, mod [L] uint8,
+ *   gate [n_mod][d] fp32 -> out [L][d] bf16.  out may alias x_res (each element
+ *   is read before it is written by the same thread); it must not alias O.
+ */
+h3_status h3_out_proj_gated_residual(const uint16_t* O, const uint16_t* Wo,
+                                     const uint16_t* x_res, const uint8_t* mod,
+                                     const float* gate, int32_t L, int32_t d, int32_t n_mod,
+                                     uint16_t* out, h3_stream_t stream);
+
+/* Bytes of device workspace h3_attn_block_fwd needs for `desc`. */
+h3_status h3_workspace_size(const h3_block_desc* desc, size_t* bytes);
+
+/*
+ * The whole sub-block ([vLLM] §1: the step run 50 times over 58,758 tokens):
+ * modulate -> QKV projection with the rotary embedding applied in its
+ * epilogue -> joint attention -> output projection with gated residual, four
+ * launches on `stream`.  workspace: >= h3_workspace_size() bytes of device
+ * memory, 256-byte aligned, owned by the caller, not read before written.
+ *   x [L][d] bf16, mod [L] uint8, pos [L][3] int32, shift/scale/gate
+ *   [n_mod][d] fp32, Wqkv [3d][d] bf16, Wo [d][d] bf16 -> out [L][d] bf16.
+ *   out may alias x.
+ */
+h3_status h3_attn_block_fwd(const h3_block_desc* desc, const uint16_t* x, const uint8_t* mod,
+                            const int32_t* pos, const float* shift, const float* scale,
+                            const float* gate, const uint16_t* Wqkv, const uint16_t* Wo,
+                            void* workspace, size_t workspace_bytes, uint16_t* out,
+                            h3_stream_t stream);
+
+/*
+ * h3_attn_block_fwd that also records five caller-created CUDA events
+ * (cudaEvent_t[5], created on the current device) on `stream`: before the
+ * first launch and after each of the four launches (modulate, QKV projection
+ * + RoPE, attention, output projection), so the caller can time each kernel
+ * inside a running step.  events == NULL behaves exactly like
+ * h3_attn_block_fwd.
+ */
+h3_status h3_attn_block_fwd_profiled(const h3_block_desc* desc, const uint16_t* x,
+                                     const uint8_t* mod, const int32_t* pos, const float* shift,
+                                     const float* scale, const float* gate, const uint16_t* Wqkv,
+                                     const uint16_t* Wo, void* workspace, size_t workspace_bytes,
+                                     uint16_t* out, h3_stream_t stream, void* const* events);
+
+/*
+ * Synchronise `stream`, then report and clear the current device's status
+ * word: H3_OK, H3_ERR_TIMEOUT, H3_ERR_BAD_INDEX or H3_ERR_CUDA.
+ */
+h3_status h3_sync_status(h3_stream_t stream);
+
+/*
+ * Upper bound, in nanoseconds of GPU global-timer time, on every wait inside
+ * the kernels (default 2e9).  A wait that exceeds it makes the kernel unwind
+ * and record H3_ERR_TIMEOUT.  0 restores the default.
+ */
+void h3_set_wait_limit_ns(uint64_t limit_ns);
+
+/*
+ * Self-test of the bounded-wait path: launches one CTA that waits on a
+ * shared-memory barrier nothing arrives on, with the given limit.  The wait
+ * must run out and the following h3_sync_status() must return H3_ERR_TIMEOUT.
+ */
+h3_status h3_selftest_wait_timeout(uint64_t limit_ns, h3_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* H3ATTN_H_ */

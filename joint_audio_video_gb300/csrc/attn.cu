@@ -1,0 +1,376 @@
+// Joint attention over the whole packed sequence on tcgen05 / TMEM.
+//
+//   O[n, h] = softmax_j(q_n . k_j * sm_scale [j <= n if causal]) v_j,  j in [0, L)
+//
+// "Joint Audio-Video Generation in Production", §1 Unified Architecture (all
+// modalities share one attention context at every step) and §6 Boundary
+// Trimming for Packed Attention (only the L effective tokens may take part:
+// keys >= L are masked here, nothing is padded); "多模态强化学习工程解析…",
+// 三 目标模型 (causal attention over the packed sequence, kept as an option).
+//
+// One CTA = one head x 256 query rows, as two 128-row tiles Q0, Q1 that share
+// every K/V block fetched.  320 threads:
+//   warp 0      TMA producer: Q0|Q1 once, then K_j, V_j (128 x 128 bf16 each,
+//               two 64-column boxes with 128-byte swizzle) into a 4-slot ring
+//   warp 1      TMEM owner + single-thread tcgen05.mma issuer
+//   warps 2..5  softmax warpgroup of tile 0 (one query row per thread)
+//   warps 6..9  softmax warpgroup of tile 1
+// Tensor memory (512 columns): S0 | S1 | O0 | O1, 128 fp32 columns each.  The
+// softmax writes P (bf16 pairs) over the first 64 columns of its S buffer and
+// the P.V product reads it from TMEM as the A operand; V is the MN-major B
+// operand straight from the TMA tile.
+// MMA order per key block j:  P0V(j-1), S0(j), P1V(j-1), S1(j), so the tensor
+// core computes one tile's products while the other tile's softmax runs.
+// Softmax works in the log2 domain with a per-row running maximum that is
+// only moved (and O, l rescaled in TMEM) when the block maximum exceeds it by
+// more than 8 (factor 256): the final O / l is exact for any such maximum.
+#include <cuda_bf16.h>
+
+#include "kernels.hpp"
+#include "ptx.cuh"
+#include "tmap.hpp"
+
+namespace h3 {
+namespace {
+
+constexpr int kThreads = 320;
+constexpr int kStages = 4;
+constexpr uint32_t kTile = 128 * 128 * 2;     // one 128x128 bf16 tile (two 16 KB boxes)
+constexpr uint32_t kBox = 128 * 64 * 2;
+constexpr size_t kSmem = 2 * kTile + kStages * kTile + 1024;
+constexpr float kRescaleThreshold = 8.0f;     // log2 units
+
+struct AttnDev {
+  __nv_bfloat16* O;
+  float* lse;
+  int L, H, d;
+  int causal;
+  float scale_log2;   // sm_scale * log2(e)
+  int num_pairs;
+  int* status;
+  uint64_t wait_ns;
+};
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ void s_product(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem) {
+  constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 0, 0);
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const uint32_t off = (k >> 2) * kBox + (k & 3) * 32;
+    mma_bf16_ss(d_tmem, sdesc_sw128(q_smem + off, 16, 1024), sdesc_sw128(k_smem + off, 16, 1024),
+                idesc, k > 0);
+  }
+}
+
+__device__ __forceinline__ void pv_product(uint32_t o_tmem, uint32_t p_tmem, uint32_t v_smem,
+                                           bool accumulate) {
+  constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 0, 1);
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    mma_bf16_ts(o_tmem, p_tmem + k * 8, sdesc_sw128(v_smem + k * 2048, kBox, 1024), idesc,
+                accumulate || k > 0);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tm, const __grid_constant__ AttnDev p) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t bar_q, bar_kv_full[kStages], bar_kv_empty[kStages], bar_s[2], bar_p[2],
+      bar_o, bar_drain;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_flag;
+
+  const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const uint32_t sQ = base;                 // Q0 at sQ, Q1 at sQ + kTile
+  const uint32_t sRing = base + 2 * kTile;
+  const int warp = warp_id();
+  const WaitCtx wc{&abort_flag, p.status, p.wait_ns};
+
+  int pair = blockIdx.x % p.num_pairs;
+  const int h = blockIdx.x / p.num_pairs;
+  if (p.causal) pair = p.num_pairs - 1 - pair;   // longest rows first
+  const int q0 = pair * 256;
+  const int kv_end = p.causal ? min(p.L, q0 + 256) : p.L;
+  const int nblk = (kv_end + 127) / 128;
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(smem_u32(&bar_q), 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_u32(&bar_kv_full[s]), 1);
+      mbar_init(smem_u32(&bar_kv_empty[s]), 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(smem_u32(&bar_s[t]), 1);
+      mbar_init(smem_u32(&bar_p[t]), 128);
+    }
+    mbar_init(smem_u32(&bar_o), 1);
+    mbar_init(smem_u32(&bar_drain), 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&tmem_base_sh), 512);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane_id() == 0) tma_prefetch_desc(&tm);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane_id() == 0) {
+      const int xq = h * 128, xk = p.d + h * 128, xv = 2 * p.d + h * 128;
+      const uint32_t qb = smem_u32(&bar_q);
+      mbar_arrive_expect_tx(qb, 2 * kTile);
+      tma_load_2d(sQ, &tm, qb, xq, q0);
+      tma_load_2d(sQ + kBox, &tm, qb, xq + 64, q0);
+      tma_load_2d(sQ + kTile, &tm, qb, xq, q0 + 128);
+      tma_load_2d(sQ + kTile + kBox, &tm, qb, xq + 64, q0 + 128);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int j = 0; j < nblk && ok; ++j) {
+        for (int kv = 0; kv < 2; ++kv) {
+          if (!mbar_wait(smem_u32(&bar_kv_empty[stage]), phase ^ 1u, wc)) { ok = false; break; }
+          const uint32_t fb = smem_u32(&bar_kv_full[stage]);
+          const uint32_t dst = sRing + stage * kTile;
+          const int x = kv == 0 ? xk : xv;
+          mbar_arrive_expect_tx(fb, kTile);
+          tma_load_2d(dst, &tm, fb, x, j * 128);
+          tma_load_2d(dst + kBox, &tm, fb, x + 64, j * 128);
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+      }
+      // let every copy in flight land before the CTA can exit
+      WaitCtx drain{&abort_flag, p.status, 2000000ull};
+      volatile int no_abort = 0;
+      drain.abort = &no_abort;
+      if (!ok) {
+        for (int s = 0; s < kStages; ++s) {
+          const uint32_t par = (s < stage) ? phase : (phase ^ 1u);
+          mbar_wait(smem_u32(&bar_kv_full[s]), par, drain);
+        }
+      }
+      mbar_wait(qb, 0, drain);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane_id() == 0) {
+      bool ok = mbar_wait(smem_u32(&bar_q), 0, wc);
+      auto slot = [&](int r, uint32_t& addr, uint32_t& par) {
+        addr = sRing + (r % kStages) * kTile;
+        par = (r / kStages) & 1;
+      };
+      auto kv_full = [&](int r) { return smem_u32(&bar_kv_full[r % kStages]); };
+      auto kv_empty = [&](int r) { return smem_u32(&bar_kv_empty[r % kStages]); };
+      const uint32_t tS0 = tmem, tS1 = tmem + 128, tO0 = tmem + 256, tO1 = tmem + 384;
+      uint32_t kA, kP, vA, vP;
+      if (ok) {
+        slot(0, kA, kP);
+        ok = mbar_wait(kv_full(0), kP, wc);
+      }
+      if (ok) {
+        tc_fence_after();
+        s_product(tS0, sQ, kA);
+        tc_commit(smem_u32(&bar_s[0]));
+        s_product(tS1, sQ + kTile, kA);
+        tc_commit(smem_u32(&bar_s[1]));
+        tc_commit(kv_empty(0));
+      }
+      for (int j = 1; j < nblk && ok; ++j) {
+        const uint32_t pph = (j - 1) & 1;
+        slot(2 * j, kA, kP);
+        slot(2 * j - 1, vA, vP);
+        ok = mbar_wait(kv_full(2 * j), kP, wc) && mbar_wait(kv_full(2 * j - 1), vP, wc) &&
+             mbar_wait(smem_u32(&bar_p[0]), pph, wc);
+        if (!ok) break;
+        tc_fence_after();
+        pv_product(tO0, tS0, vA, j > 1);
+        s_product(tS0, sQ, kA);
+        tc_commit(smem_u32(&bar_s[0]));
+        ok = mbar_wait(smem_u32(&bar_p[1]), pph, wc);
+        if (!ok) break;
+        tc_fence_after();
+        pv_product(tO1, tS1, vA, j > 1);
+        tc_commit(kv_empty(2 * j - 1));
+        s_product(tS1, sQ + kTile, kA);
+        tc_commit(smem_u32(&bar_s[1]));
+        tc_commit(kv_empty(2 * j));
+      }
+      if (ok) {
+        const int j = nblk;
+        const uint32_t pph = (j - 1) & 1;
+        slot(2 * j - 1, vA, vP);
+        ok = mbar_wait(kv_full(2 * j - 1), vP, wc) && mbar_wait(smem_u32(&bar_p[0]), pph, wc);
+        if (ok) {
+          tc_fence_after();
+          pv_product(tO0, tS0, vA, j > 1);
+          ok = mbar_wait(smem_u32(&bar_p[1]), pph, wc);
+        }
+        if (ok) {
+          tc_fence_after();
+          pv_product(tO1, tS1, vA, j > 1);
+          tc_commit(kv_empty(2 * j - 1));
+          tc_commit(smem_u32(&bar_o));
+        }
+      }
+      tc_commit(smem_u32(&bar_drain));
+      WaitCtx drain{&abort_flag, p.status, p.wait_ns};
+      volatile int no_abort = 0;
+      drain.abort = &no_abort;
+      mbar_wait(smem_u32(&bar_drain), 0, drain);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int g = (warp - 2) >> 2;          // tile 0 or 1
+    const int q = warp & 3;                 // TMEM lane quarter
+    const int row = q * 32 + lane_id();
+    const int tile_q0 = q0 + g * 128;
+    const int qi = tile_q0 + row;
+    const uint32_t lane_off = uint32_t(q * 32) << 16;
+    const uint32_t tS = tmem + g * 128 + lane_off;
+    const uint32_t tO = tmem + 256 + g * 128 + lane_off;
+    const uint32_t bs = smem_u32(&bar_s[g]), bp = smem_u32(&bar_p[g]);
+    float m_used = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < nblk; ++j) {
+      ok = __all_sync(0xffffffffu, mbar_wait(bs, j & 1, wc));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t r0[32], r1[32], r2[32], r3[32];
+      tmem_ld32(tS, r0);
+      tmem_ld32(tS + 32, r1);
+      tmem_ld32(tS + 64, r2);
+      tmem_ld32(tS + 96, r3);
+      tmem_ld_wait(r0);
+      tmem_ld_wait(r1);
+      tmem_ld_wait(r2);
+      tmem_ld_wait(r3);
+      float s[128];
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        s[c] = __uint_as_float(r0[c]) * p.scale_log2;
+        s[32 + c] = __uint_as_float(r1[c]) * p.scale_log2;
+        s[64 + c] = __uint_as_float(r2[c]) * p.scale_log2;
+        s[96 + c] = __uint_as_float(r3[c]) * p.scale_log2;
+      }
+      const int kv0 = j * 128;
+      const bool tail = kv0 + 128 > p.L;
+      const bool diag = p.causal && kv0 + 127 > tile_q0;
+      if (tail || diag) {
+        const int lim = p.causal ? min(p.L - 1, qi) : p.L - 1;   // last visible key
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+          if (kv0 + c > lim) s[c] = -INFINITY;
+      }
+      float mx = s[0];
+#pragma unroll
+      for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
+      if (j == 0) {
+        m_used = mx;
+      } else {
+        const float m_new = fmaxf(m_used, mx);
+        const bool need = m_new > m_used + kRescaleThreshold;
+        if (__any_sync(0xffffffffu, need)) {
+          const float f = need ? ex2(m_used - m_new) : 1.f;
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tO + c * 32, o);
+            tmem_ld_wait(o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
+            tmem_st32(tO + c * 32, o);
+          }
+          tmem_st_wait();
+          l *= f;
+          if (need) m_used = m_new;
+        }
+      }
+      uint32_t pk0[32], pk1[32];
+      float sum = 0.f;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const float a = ex2(s[2 * i] - m_used), b = ex2(s[2 * i + 1] - m_used);
+        sum += a + b;
+        pk0[i] = pack_bf16x2(a, b);
+      }
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const float a = ex2(s[64 + 2 * i] - m_used), b = ex2(s[64 + 2 * i + 1] - m_used);
+        sum += a + b;
+        pk1[i] = pack_bf16x2(a, b);
+      }
+      l += sum;
+      tmem_st32(tS, pk0);
+      tmem_st32(tS + 32, pk1);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bp);
+    }
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_o), 0, wc));
+    if (ok) {
+      tc_fence_after();
+      const float inv_l = 1.f / l;
+      __nv_bfloat16* orow = p.O + size_t(qi) * p.d + h * 128;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t o[32];
+        tmem_ld32(tO + c * 32, o);
+        tmem_ld_wait(o);
+        if (qi < p.L) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float* f = reinterpret_cast<const float*>(o + 8 * i);
+            dst[i] = make_uint4(pack_bf16x2(f[0] * inv_l, f[1] * inv_l),
+                                pack_bf16x2(f[2] * inv_l, f[3] * inv_l),
+                                pack_bf16x2(f[4] * inv_l, f[5] * inv_l),
+                                pack_bf16x2(f[6] * inv_l, f[7] * inv_l));
+          }
+        }
+      }
+      if (p.lse != nullptr && qi < p.L)
+        p.lse[size_t(h) * p.L + qi] = (m_used + __log2f(l)) * 0.69314718055994531f;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+}  // namespace
+
+cudaError_t launch_attention(const AttnArgs& a, const DevCtx& ctx, cudaStream_t st) {
+  const int d = a.H * 128;
+  CUtensorMap tm;
+  if (!make_tmap_bf16_2d(&tm, a.qkv, a.L, 3 * d, 3 * d, 128, 64)) return cudaErrorInvalidValue;
+  AttnDev p{};
+  p.O = static_cast<__nv_bfloat16*>(a.O);
+  p.lse = a.lse;
+  p.L = a.L;
+  p.H = a.H;
+  p.d = d;
+  p.causal = a.causal;
+  p.scale_log2 = a.sm_scale * 1.4426950408889634f;
+  p.num_pairs = (a.L + 255) / 256;
+  p.status = ctx.status;
+  p.wait_ns = ctx.wait_ns;
+  cudaError_t e =
+      cudaFuncSetAttribute(attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmem));
+  if (e != cudaSuccess) return e;
+  const long long grid = (long long)p.num_pairs * a.H;
+  attn_fwd_kernel<<<unsigned(grid), kThreads, kSmem, st>>>(tm, p);
+  return cudaGetLastError();
+}
+
+}  // namespace h3

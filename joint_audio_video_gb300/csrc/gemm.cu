@@ -1,0 +1,341 @@
+// Persistent tcgen05 GEMM  C[M][N] = A[M][K] * B[N][K]^T  (bf16 in, fp32 accumulate)
+// with the sub-block's fused epilogues:
+//   EPI_PLAIN           C = acc                                     (h3_qkv_proj)
+//   EPI_ROPE            Q/K columns rotated by the 3D (t,h,w) RoPE, V as is
+//                       (fused QKV projection of the block; "Joint Audio-Video
+//                       Generation in Production", §3: tags + RoPE per token)
+//   EPI_GATED_RESIDUAL  C = x_res + gate[mod] * acc                 (output projection
+//                       + AdaLN gate; "DiffusionNFT on MiniMax H3", modality-specific
+//                       AdaLN branches)
+//
+// Layout of the work (one CTA per SM, 192 threads):
+//   warp 0      TMA producer: A tile 128x64 and B tile BNx64 per k-block into a
+//               4-stage shared-memory ring (128-byte swizzle, 1 KB aligned)
+//   warp 1      TMEM allocation + one elected thread issuing tcgen05.mma
+//               (M=128, N=BN, K=16 per instruction) into one of two TMEM
+//               accumulators (2 x BN fp32 columns)
+//   warps 2..5  epilogue: tcgen05.ld of one accumulator row per thread, fused
+//               epilogue math in fp32, bf16 stores; releases the accumulator
+//               so the MMA of the next tile overlaps this epilogue
+// Tiles are visited in groups of kGroupM row-tiles (all N tiles of a group
+// before the next group), so the working set of A and B stays in L2.
+#include <cuda_bf16.h>
+
+#include "kernels.hpp"
+#include "ptx.cuh"
+#include "tmap.hpp"
+
+namespace h3 {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int kThreads = 192;
+constexpr int kGroupM = 16;
+
+template <int BN>
+struct GemmCfg {
+  static constexpr int kStages = BN == 256 ? 4 : 6;
+  static constexpr uint32_t kABytes = BM * BK * 2;
+  static constexpr uint32_t kBBytes = BN * BK * 2;
+  static constexpr uint32_t kStageBytes = kABytes + kBBytes;
+  static constexpr uint32_t kTmemCols = 2 * BN;  // two accumulators
+  static constexpr size_t kSmem = size_t(kStages) * kStageBytes + 1024;
+};
+
+struct GemmDev {
+  __nv_bfloat16* C;
+  int M, N, K;
+  int num_m, num_n;
+  const int32_t* pos;
+  int d;
+  const __nv_bfloat16* x_res;
+  const uint8_t* mod;
+  const float* gate;
+  int n_mod;
+  int* status;
+  uint64_t wait_ns;
+};
+
+__device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int& mb, int& nb) {
+  const int per_group = kGroupM * num_n;
+  const int g = t / per_group;
+  const int first_m = g * kGroupM;
+  const int gsz = min(num_m - first_m, kGroupM);
+  const int r = t - g * per_group;
+  mb = first_m + r % gsz;
+  nb = r / gsz;
+}
+
+// Epilogue of one 32-column chunk held in r[] (fp32 bits) for row `grow`,
+// global columns gc .. gc+31.
+template <int EPI>
+__device__ __forceinline__ void epilogue_chunk(const GemmDev& p, const RopeTable& rt,
+                                               uint32_t (&r)[32], int grow, int gc,
+                                               const int32_t (&pr)[3], int m) {
+  float v[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+  if constexpr (EPI == EPI_ROPE) {
+    if (gc < 2 * p.d) {   // Q or K block: rotate pairs (2k, 2k+1) of the head
+      const int k0 = (gc & 127) >> 1;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int k = k0 + j;
+        const int ax = rt.axis[k];
+        const int pa = ax == 0 ? pr[0] : (ax == 1 ? pr[1] : pr[2]);
+        const float ang = float(pa) * rt.inv_freq[k];
+        float s, c;
+        sincosf(ang, &s, &c);
+        const float a = v[2 * j], b = v[2 * j + 1];
+        v[2 * j] = a * c - b * s;
+        v[2 * j + 1] = a * s + b * c;
+      }
+    }
+  }
+  __nv_bfloat16* crow = p.C + size_t(grow) * p.N + gc;
+  if constexpr (EPI == EPI_GATED_RESIDUAL) {
+    const uint4* xr = reinterpret_cast<const uint4*>(p.x_res + size_t(grow) * p.N + gc);
+    const float4* gr = reinterpret_cast<const float4*>(p.gate + size_t(m) * p.N + gc);
+    uint4 xv[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) xv[i] = xr[i];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float4 g = __ldg(gr + i);
+      const uint32_t w0 = (&xv[i >> 1].x)[(i & 1) * 2];
+      const uint32_t w1 = (&xv[i >> 1].x)[(i & 1) * 2 + 1];
+      v[4 * i + 0] = fmaf(g.x, v[4 * i + 0], __uint_as_float(w0 << 16));
+      v[4 * i + 1] = fmaf(g.y, v[4 * i + 1], __uint_as_float(w0 & 0xFFFF0000u));
+      v[4 * i + 2] = fmaf(g.z, v[4 * i + 2], __uint_as_float(w1 << 16));
+      v[4 * i + 3] = fmaf(g.w, v[4 * i + 3], __uint_as_float(w1 & 0xFFFF0000u));
+    }
+  }
+  uint4* out = reinterpret_cast<uint4*>(crow);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    out[i] = make_uint4(pack_bf16x2(v[8 * i + 0], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
+                        pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
+  }
+}
+
+template <int BN, int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const __grid_constant__ GemmDev p, const __grid_constant__ RopeTable rt) {
+  using Cfg = GemmCfg<BN>;
+  constexpr int S = Cfg::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t bar_full[S], bar_empty[S], bar_acc_full[2], bar_acc_empty[2], bar_drain;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_flag;
+
+  const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const int warp = warp_id();
+  const WaitCtx wc{&abort_flag, p.status, p.wait_ns};
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    for (int s = 0; s < S; ++s) {
+      mbar_init(smem_u32(&bar_full[s]), 1);
+      mbar_init(smem_u32(&bar_empty[s]), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(smem_u32(&bar_acc_full[a]), 1);
+      mbar_init(smem_u32(&bar_acc_empty[a]), 128);
+    }
+    mbar_init(smem_u32(&bar_drain), 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&tmem_base_sh), Cfg::kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane_id() == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+
+  const int num_tiles = p.num_m * p.num_n;
+  const int kblocks = p.K / BK;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- producer
+    if (lane_id() == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+        int mb, nb;
+        tile_coords(t, p.num_m, p.num_n, mb, nb);
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(smem_u32(&bar_empty[stage]), phase ^ 1u, wc)) { ok = false; break; }
+          const uint32_t fb = smem_u32(&bar_full[stage]);
+          const uint32_t sa = base + stage * Cfg::kStageBytes;
+          mbar_arrive_expect_tx(fb, Cfg::kStageBytes);
+          tma_load_2d(sa, &tmA, fb, kb * BK, mb * BM);
+          tma_load_2d(sa + Cfg::kABytes, &tmB, fb, kb * BK, nb * BN);
+          if (++stage == S) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (!ok) {
+        // unwind: let copies already in flight land before the CTA exits
+        WaitCtx drain{&abort_flag, p.status, 2000000ull};
+        volatile int no_abort = 0;
+        drain.abort = &no_abort;
+        for (int s = 0; s < S; ++s) {
+          // a stage is in flight iff its full barrier is one phase behind the ring
+          const uint32_t par = (s < stage) ? phase : (phase ^ 1u);
+          mbar_wait(smem_u32(&bar_full[s]), par, drain);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane_id() == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, 0, 0);
+      int stage = 0;
+      uint32_t phase = 0;
+      int it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++it) {
+        const int acc = it & 1;
+        const uint32_t acc_phase = (it >> 1) & 1;
+        if (!mbar_wait(smem_u32(&bar_acc_empty[acc]), acc_phase ^ 1u, wc)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t dtm = tmem + acc * BN;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(smem_u32(&bar_full[stage]), phase, wc)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sa = base + stage * Cfg::kStageBytes;
+          const uint32_t sb = sa + Cfg::kABytes;
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            mma_bf16_ss(dtm, sdesc_sw128(sa + k * 32, 16, 1024), sdesc_sw128(sb + k * 32, 16, 1024),
+                        idesc, (kb | k) != 0);
+          }
+          tc_commit(smem_u32(&bar_empty[stage]));
+          if (++stage == S) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        tc_commit(smem_u32(&bar_acc_full[acc]));
+      }
+      // drain: every MMA issued so far has finished before TMEM is released
+      tc_commit(smem_u32(&bar_drain));
+      WaitCtx drain{&abort_flag, p.status, p.wait_ns};
+      volatile int no_abort = 0;
+      drain.abort = &no_abort;
+      mbar_wait(smem_u32(&bar_drain), 0, drain);
+    }
+  } else {
+    // ---------------------------------------------------------------- epilogue
+    const int q = warp & 3;                 // TMEM lane quarter of this warp
+    const int row_in_tile = q * 32 + lane_id();
+    int it = 0;
+    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++it) {
+      int mb, nb;
+      tile_coords(t, p.num_m, p.num_n, mb, nb);
+      const int acc = it & 1;
+      const uint32_t acc_phase = (it >> 1) & 1;
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_acc_full[acc]), acc_phase, wc));
+      if (!ok) break;
+      tc_fence_after();
+      const int grow = mb * BM + row_in_tile;
+      const bool live = grow < p.M;
+      int32_t pr[3] = {0, 0, 0};
+      int m = 0;
+      if constexpr (EPI == EPI_ROPE) {
+        if (live) {
+          pr[0] = p.pos[size_t(grow) * 3 + 0];
+          pr[1] = p.pos[size_t(grow) * 3 + 1];
+          pr[2] = p.pos[size_t(grow) * 3 + 2];
+        }
+      }
+      bool bad = false;
+      if constexpr (EPI == EPI_GATED_RESIDUAL) {
+        if (live) {
+          m = p.mod[grow];
+          if (m >= p.n_mod) { bad = true; m = 0; }
+        }
+      }
+      const uint32_t tacc = tmem + acc * BN + (uint32_t(q * 32) << 16);
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tacc + c * 32, r);
+        tmem_ld_wait(r);
+        if (live) {
+          if (bad) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = 0x7FC00000u;   // NaN row
+          }
+          epilogue_chunk<EPI>(p, rt, r, grow, nb * BN + c * 32, pr, m);
+        }
+      }
+      if (bad) atomicCAS(p.status, H3_DEV_OK, H3_DEV_BAD_INDEX);
+      tc_fence_before();
+      mbar_arrive(smem_u32(&bar_acc_empty[acc]));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, Cfg::kTmemCols);
+}
+
+template <int BN, int EPI>
+cudaError_t launch_typed(const GemmArgs& a, const DevCtx& ctx, cudaStream_t st) {
+  using Cfg = GemmCfg<BN>;
+  CUtensorMap tmA, tmB;
+  if (!make_tmap_bf16_2d(&tmA, a.A, a.M, a.K, a.K, BM, BK)) return cudaErrorInvalidValue;
+  if (!make_tmap_bf16_2d(&tmB, a.B, a.N, a.K, a.K, BN, BK)) return cudaErrorInvalidValue;
+  GemmDev p{};
+  p.C = static_cast<__nv_bfloat16*>(a.C);
+  p.M = a.M;
+  p.N = a.N;
+  p.K = a.K;
+  p.num_m = (a.M + BM - 1) / BM;
+  p.num_n = a.N / BN;
+  p.pos = a.pos;
+  p.d = a.d;
+  p.x_res = static_cast<const __nv_bfloat16*>(a.x_res);
+  p.mod = a.mod;
+  p.gate = a.gate;
+  p.n_mod = a.n_mod;
+  p.status = ctx.status;
+  p.wait_ns = ctx.wait_ns;
+  RopeTable rt{};
+  if (a.rope) rt = *a.rope;
+  auto kern = gemm_kernel<BN, EPI>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       int(Cfg::kSmem));
+  if (e != cudaSuccess) return e;
+  const int tiles = p.num_m * p.num_n;
+  const int grid = tiles < ctx.num_sms ? tiles : ctx.num_sms;
+  kern<<<grid, kThreads, Cfg::kSmem, st>>>(tmA, tmB, p, rt);
+  return cudaGetLastError();
+}
+
+template <int BN>
+cudaError_t launch_bn(const GemmArgs& a, const DevCtx& ctx, cudaStream_t st) {
+  switch (a.epilogue) {
+    case EPI_PLAIN: return launch_typed<BN, EPI_PLAIN>(a, ctx, st);
+    case EPI_ROPE: return launch_typed<BN, EPI_ROPE>(a, ctx, st);
+    case EPI_GATED_RESIDUAL: return launch_typed<BN, EPI_GATED_RESIDUAL>(a, ctx, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(const GemmArgs& a, const DevCtx& ctx, cudaStream_t st) {
+  if (a.N % 256 == 0) return launch_bn<256>(a, ctx, st);
+  return launch_bn<128>(a, ctx, st);
+}
+
+}  // namespace h3

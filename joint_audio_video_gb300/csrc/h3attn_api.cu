@@ -1,0 +1,358 @@
+// C ABI of the joint audio-video attention sub-block (include/h3attn.h).
+//
+// Every entry point validates its arguments on the host and returns an
+// h3_status before anything is launched; launches go to the caller's stream.
+// Kernels report asynchronous problems (bounded wait ran out, modality id out
+// of range) through one status word per device, read by h3_sync_status().
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "../../include/h3attn.h"
+#include "kernels.hpp"
+#include "ptx.cuh"
+
+namespace h3 {
+
+__device__ int g_status_word;
+
+namespace {
+
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;
+constexpr int kMaxDevices = 64;
+std::atomic<uint64_t> g_wait_ns{kDefaultWaitNs};
+
+struct DevInfo {
+  std::atomic<int> ready{0};
+  int* status = nullptr;
+  int num_sms = 0;
+};
+DevInfo g_dev[kMaxDevices];
+
+h3_status dev_ctx(DevCtx* ctx) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return H3_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return H3_ERR_UNSUPPORTED;
+  DevInfo& di = g_dev[dev];
+  if (!di.ready.load(std::memory_order_acquire)) {
+    void* p = nullptr;
+    int sms = 0;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return H3_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return H3_ERR_CUDA;
+    di.status = static_cast<int*>(p);
+    di.num_sms = sms;
+    di.ready.store(1, std::memory_order_release);
+  }
+  ctx->status = di.status;
+  ctx->num_sms = di.num_sms;
+  ctx->wait_ns = g_wait_ns.load(std::memory_order_relaxed);
+  return H3_OK;
+}
+
+bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlap(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+bool valid_d(int32_t d) { return d >= 128 && d <= 16384 && d % 128 == 0; }
+
+h3_status launched(cudaError_t e) { return e == cudaSuccess ? H3_OK : H3_ERR_CUDA; }
+
+h3_status check_rope(const int32_t sec[3], int32_t head_dim, float base) {
+  if (sec == nullptr) return H3_ERR_INVALID_ARG;
+  int sum = 0;
+  for (int a = 0; a < 3; ++a) {
+    if (sec[a] < 0 || sec[a] % 2 != 0) return H3_ERR_INVALID_ARG;
+    sum += sec[a];
+  }
+  if (sum != head_dim) return H3_ERR_INVALID_ARG;
+  if (!(base > 0.f) || !std::isfinite(base)) return H3_ERR_INVALID_ARG;
+  return H3_OK;
+}
+
+size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// ------------------------------------------------------------------ self-test kernel
+__global__ void wait_selftest_kernel(int* status, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(smem_u32(&bar), 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  const WaitCtx wc{&abort_flag, status, limit_ns};
+  // nothing ever arrives on `bar`: the wait must run out and record a timeout
+  mbar_wait(smem_u32(&bar), 0, wc);
+}
+
+}  // namespace
+
+cudaError_t launch_wait_selftest(const DevCtx& ctx, cudaStream_t st) {
+  wait_selftest_kernel<<<1, 32, 0, st>>>(ctx.status, ctx.wait_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace h3
+
+using namespace h3;
+
+extern "C" {
+
+const char* h3_status_string(h3_status s) {
+  switch (s) {
+    case H3_OK: return "ok";
+    case H3_ERR_INVALID_ARG: return "invalid argument (nothing launched)";
+    case H3_ERR_UNSUPPORTED: return "unsupported shape or option (nothing launched)";
+    case H3_ERR_CUDA: return "CUDA runtime error";
+    case H3_ERR_TIMEOUT: return "a kernel gave up on a bounded wait";
+    case H3_ERR_BAD_INDEX: return "modality id out of range";
+    case H3_ERR_WORKSPACE: return "workspace too small";
+    default: return "unknown status";
+  }
+}
+
+const char* h3_version(void) { return "h3attn 0.1.0 sm_103a"; }
+
+void h3_set_wait_limit_ns(uint64_t limit_ns) {
+  g_wait_ns.store(limit_ns == 0 ? kDefaultWaitNs : limit_ns, std::memory_order_relaxed);
+}
+
+h3_status h3_adaln_modulate(const uint16_t* x, const uint8_t* mod, const float* shift,
+                            const float* scale, int32_t L, int32_t d, int32_t n_mod, float eps,
+                            uint16_t* y, h3_stream_t stream) {
+  if (L < 1 || !valid_d(d) || n_mod < 1 || n_mod > 255) return H3_ERR_INVALID_ARG;
+  if (!(eps >= 0.f) || !std::isfinite(eps)) return H3_ERR_INVALID_ARG;
+  if (!aligned16(x) || mod == nullptr || !aligned16(shift) || !aligned16(scale) || !aligned16(y))
+    return H3_ERR_INVALID_ARG;
+  const size_t bytes = size_t(L) * d * 2;
+  if (x != y && overlap(x, bytes, y, bytes)) return H3_ERR_INVALID_ARG;
+  DevCtx ctx;
+  if (h3_status s = dev_ctx(&ctx)) return s;
+  return launched(launch_adaln_modulate(x, mod, shift, scale, L, d, n_mod, eps, y, ctx,
+                                        reinterpret_cast<cudaStream_t>(stream)));
+}
+
+h3_status h3_qkv_proj(const uint16_t* y, const uint16_t* Wqkv, int32_t L, int32_t d, uint16_t* qkv,
+                      h3_stream_t stream) {
+  if (L < 1 || !valid_d(d)) return H3_ERR_INVALID_ARG;
+  if (!aligned16(y) || !aligned16(Wqkv) || !aligned16(qkv)) return H3_ERR_INVALID_ARG;
+  if (overlap(y, size_t(L) * d * 2, qkv, size_t(L) * 3 * d * 2)) return H3_ERR_INVALID_ARG;
+  DevCtx ctx;
+  if (h3_status s = dev_ctx(&ctx)) return s;
+  GemmArgs a{};
+  a.A = y;
+  a.B = Wqkv;
+  a.C = qkv;
+  a.M = L;
+  a.N = 3 * d;
+  a.K = d;
+  a.epilogue = EPI_PLAIN;
+  return launched(launch_gemm(a, ctx, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+h3_status h3_mrope_apply(uint16_t* qkv, const int32_t* pos, int32_t L, int32_t n_heads,
+                         int32_t head_dim, const int32_t sec[3], float base, h3_stream_t stream) {
+  if (L < 1 || n_heads < 1) return H3_ERR_INVALID_ARG;
+  if (head_dim != 128) return H3_ERR_UNSUPPORTED;
+  if (!valid_d(n_heads * 128)) return H3_ERR_INVALID_ARG;
+  if (h3_status s = check_rope(sec, head_dim, base)) return s;
+  if (!aligned16(qkv) || pos == nullptr || (reinterpret_cast<uintptr_t>(pos) & 3u))
+    return H3_ERR_INVALID_ARG;
+  DevCtx ctx;
+  if (h3_status s = dev_ctx(&ctx)) return s;
+  RopeTable rt;
+  make_rope_table(&rt, sec, base);
+  return launched(launch_mrope(qkv, pos, L, n_heads, rt, ctx, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+h3_status h3_joint_attn_fwd(const uint16_t* qkv, int32_t L, int32_t n_heads, int32_t head_dim,
+                            int32_t causal, float sm_scale, uint16_t* O, float* lse,
+                            h3_stream_t stream) {
+  if (L < 1 || n_heads < 1) return H3_ERR_INVALID_ARG;
+  if (head_dim != 128) return H3_ERR_UNSUPPORTED;
+  if (!valid_d(n_heads * 128)) return H3_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return H3_ERR_INVALID_ARG;
+  if (!(sm_scale > 0.f) || !std::isfinite(sm_scale)) return H3_ERR_INVALID_ARG;
+  if (!aligned16(qkv) || !aligned16(O)) return H3_ERR_INVALID_ARG;
+  if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u)) return H3_ERR_INVALID_ARG;
+  const size_t d = size_t(n_heads) * 128;
+  if (overlap(qkv, size_t(L) * 3 * d * 2, O, size_t(L) * d * 2)) return H3_ERR_INVALID_ARG;
+  DevCtx ctx;
+  if (h3_status s = dev_ctx(&ctx)) return s;
+  AttnArgs a{};
+  a.qkv = qkv;
+  a.O = O;
+  a.lse = lse;
+  a.L = L;
+  a.H = n_heads;
+  a.causal = causal;
+  a.sm_scale = sm_scale;
+  return launched(launch_attention(a, ctx, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+h3_status h3_out_proj_gated_residual(const uint16_t* O, const uint16_t* Wo,
+                                     const uint16_t* x_res, const uint8_t* mod,
+                                     const float* gate, int32_t L, int32_t d, int32_t n_mod,
+                                     uint16_t* out, h3_stream_t stream) {
+  if (L < 1 || !valid_d(d) || n_mod < 1 || n_mod > 255) return H3_ERR_INVALID_ARG;
+  if (!aligned16(O) || !aligned16(Wo) || !aligned16(x_res) || mod == nullptr ||
+      !aligned16(gate) || !aligned16(out))
+    return H3_ERR_INVALID_ARG;
+  const size_t bytes = size_t(L) * d * 2;
+  if (overlap(O, bytes, out, bytes)) return H3_ERR_INVALID_ARG;
+  if (x_res != out && overlap(x_res, bytes, out, bytes)) return H3_ERR_INVALID_ARG;
+  DevCtx ctx;
+  if (h3_status s = dev_ctx(&ctx)) return s;
+  GemmArgs a{};
+  a.A = O;
+  a.B = Wo;
+  a.C = out;
+  a.M = L;
+  a.N = d;
+  a.K = d;
+  a.epilogue = EPI_GATED_RESIDUAL;
+  a.x_res = x_res;
+  a.mod = mod;
+  a.gate = gate;
+  a.n_mod = n_mod;
+  return launched(launch_gemm(a, ctx, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+static h3_status check_desc(const h3_block_desc* desc) {
+  if (desc == nullptr) return H3_ERR_INVALID_ARG;
+  if (desc->L < 1 || desc->n_heads < 1 || desc->n_mod < 1 || desc->n_mod > 255)
+    return H3_ERR_INVALID_ARG;
+  if (desc->head_dim != 128) return H3_ERR_UNSUPPORTED;
+  if (desc->d != desc->n_heads * desc->head_dim || !valid_d(desc->d)) return H3_ERR_INVALID_ARG;
+  if (desc->causal != 0 && desc->causal != 1) return H3_ERR_INVALID_ARG;
+  if (!(desc->ln_eps >= 0.f) || !std::isfinite(desc->ln_eps)) return H3_ERR_INVALID_ARG;
+  return check_rope(desc->rope_sec, desc->head_dim, desc->rope_base);
+}
+
+h3_status h3_workspace_size(const h3_block_desc* desc, size_t* bytes) {
+  if (bytes == nullptr) return H3_ERR_INVALID_ARG;
+  if (h3_status s = check_desc(desc)) return s;
+  const size_t L = size_t(desc->L), d = size_t(desc->d);
+  *bytes = round256(L * d * 2) + round256(L * 3 * d * 2);
+  return H3_OK;
+}
+
+h3_status h3_attn_block_fwd(const h3_block_desc* desc, const uint16_t* x, const uint8_t* mod,
+                            const int32_t* pos, const float* shift, const float* scale,
+                            const float* gate, const uint16_t* Wqkv, const uint16_t* Wo,
+                            void* workspace, size_t workspace_bytes, uint16_t* out,
+                            h3_stream_t stream) {
+  return h3_attn_block_fwd_profiled(desc, x, mod, pos, shift, scale, gate, Wqkv, Wo, workspace,
+                                    workspace_bytes, out, stream, nullptr);
+}
+
+h3_status h3_attn_block_fwd_profiled(const h3_block_desc* desc, const uint16_t* x,
+                                     const uint8_t* mod, const int32_t* pos, const float* shift,
+                                     const float* scale, const float* gate, const uint16_t* Wqkv,
+                                     const uint16_t* Wo, void* workspace, size_t workspace_bytes,
+                                     uint16_t* out, h3_stream_t stream, void* const* events) {
+  size_t need = 0;
+  if (h3_status s = h3_workspace_size(desc, &need)) return s;
+  if (!aligned16(x) || mod == nullptr || pos == nullptr || (reinterpret_cast<uintptr_t>(pos) & 3u) ||
+      !aligned16(shift) || !aligned16(scale) || !aligned16(gate) || !aligned16(Wqkv) ||
+      !aligned16(Wo) || !aligned16(out) || workspace == nullptr ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return H3_ERR_INVALID_ARG;
+  if (workspace_bytes < need) return H3_ERR_WORKSPACE;
+  const size_t L = size_t(desc->L), d = size_t(desc->d);
+  const size_t xbytes = L * d * 2;
+  if (x != out && overlap(x, xbytes, out, xbytes)) return H3_ERR_INVALID_ARG;
+  if (overlap(workspace, need, x, xbytes) || overlap(workspace, need, out, xbytes))
+    return H3_ERR_INVALID_ARG;
+  DevCtx ctx;
+  if (h3_status s = dev_ctx(&ctx)) return s;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  void* y = ws;                              // y, later reused for O
+  void* qkv = ws + round256(L * d * 2);
+  const int Li = desc->L, di = desc->d;
+  auto mark = [&](int i) -> bool {
+    return events == nullptr ||
+           cudaEventRecord(static_cast<cudaEvent_t>(events[i]), st) == cudaSuccess;
+  };
+  if (!mark(0)) return H3_ERR_CUDA;
+
+  cudaError_t e = launch_adaln_modulate(x, mod, shift, scale, Li, di, desc->n_mod, desc->ln_eps, y,
+                                        ctx, st);
+  if (e != cudaSuccess || !mark(1)) return H3_ERR_CUDA;
+
+  RopeTable rt;
+  make_rope_table(&rt, desc->rope_sec, desc->rope_base);
+  GemmArgs g{};
+  g.A = y;
+  g.B = Wqkv;
+  g.C = qkv;
+  g.M = Li;
+  g.N = 3 * di;
+  g.K = di;
+  g.epilogue = EPI_ROPE;
+  g.pos = pos;
+  g.d = di;
+  g.rope = &rt;
+  if (launch_gemm(g, ctx, st) != cudaSuccess || !mark(2)) return H3_ERR_CUDA;
+
+  AttnArgs a{};
+  a.qkv = qkv;
+  a.O = y;
+  a.lse = nullptr;
+  a.L = Li;
+  a.H = desc->n_heads;
+  a.causal = desc->causal;
+  a.sm_scale = 1.0f / std::sqrt(float(desc->head_dim));
+  if (launch_attention(a, ctx, st) != cudaSuccess || !mark(3)) return H3_ERR_CUDA;
+
+  GemmArgs o{};
+  o.A = y;
+  o.B = Wo;
+  o.C = out;
+  o.M = Li;
+  o.N = di;
+  o.K = di;
+  o.epilogue = EPI_GATED_RESIDUAL;
+  o.x_res = x;
+  o.mod = mod;
+  o.gate = gate;
+  o.n_mod = desc->n_mod;
+  if (launch_gemm(o, ctx, st) != cudaSuccess || !mark(4)) return H3_ERR_CUDA;
+  return H3_OK;
+}
+
+h3_status h3_sync_status(h3_stream_t stream) {
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return H3_ERR_CUDA;
+  DevCtx ctx;
+  if (h3_status s = dev_ctx(&ctx)) return s;
+  int v = 0;
+  if (cudaMemcpy(&v, ctx.status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return H3_ERR_CUDA;
+  if (v != H3_DEV_OK && cudaMemset(ctx.status, 0, sizeof(int)) != cudaSuccess) return H3_ERR_CUDA;
+  switch (v) {
+    case H3_DEV_OK: return H3_OK;
+    case H3_DEV_TIMEOUT: return H3_ERR_TIMEOUT;
+    case H3_DEV_BAD_INDEX: return H3_ERR_BAD_INDEX;
+    default: return H3_ERR_CUDA;
+  }
+}
+
+h3_status h3_selftest_wait_timeout(uint64_t limit_ns, h3_stream_t stream) {
+  if (limit_ns == 0 || limit_ns > 10000000000ull) return H3_ERR_INVALID_ARG;
+  DevCtx ctx;
+  if (h3_status s = dev_ctx(&ctx)) return s;
+  ctx.wait_ns = limit_ns;
+  return launched(launch_wait_selftest(ctx, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

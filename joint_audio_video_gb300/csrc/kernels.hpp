@@ -1,0 +1,67 @@
+// Internal launch interface between the C ABI (h3attn_api.cu) and the kernels.
+// Every launcher returns the launch's cudaError_t; arguments are validated by
+// the caller before any launcher runs.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace h3 {
+
+struct DevCtx {
+  int* status;          // device status word
+  uint64_t wait_ns;     // bound on every in-kernel wait
+  int num_sms;
+};
+
+// Per-pair rotary table: pair k of a head covers dims (2k, 2k+1).
+struct RopeTable {
+  float inv_freq[64];   // base^(-2j/n_a), computed in double, rounded once
+  int32_t axis[64];     // 0 = t, 1 = h, 2 = w
+};
+
+// Fills `rt` for sections sec[0..2] (even, summing to 128) and `base`.
+void make_rope_table(RopeTable* rt, const int32_t sec[3], double base);
+
+cudaError_t launch_adaln_modulate(const void* x, const uint8_t* mod, const float* shift,
+                                  const float* scale, int L, int d, int n_mod, float eps, void* y,
+                                  const DevCtx& ctx, cudaStream_t st);
+
+cudaError_t launch_mrope(void* qkv, const int32_t* pos, int L, int n_heads, const RopeTable& rt,
+                         const DevCtx& ctx, cudaStream_t st);
+
+enum GemmEpilogue : int { EPI_PLAIN = 0, EPI_ROPE = 1, EPI_GATED_RESIDUAL = 2 };
+
+struct GemmArgs {
+  const void* A;        // [M][K] bf16, row-major
+  const void* B;        // [N][K] bf16, row-major (nn.Linear weight)
+  void* C;              // [M][N] bf16
+  int M, N, K;
+  int epilogue;         // GemmEpilogue
+  // EPI_ROPE: Q block = columns [0, d), K block = [d, 2d); V untouched
+  const int32_t* pos;   // [M][3]
+  int d;
+  const RopeTable* rope;
+  // EPI_GATED_RESIDUAL: C = x_res + gate[mod] * (A B^T)
+  const void* x_res;    // [M][N] bf16
+  const uint8_t* mod;   // [M]
+  const float* gate;    // [n_mod][N]
+  int n_mod;
+};
+
+cudaError_t launch_gemm(const GemmArgs& a, const DevCtx& ctx, cudaStream_t st);
+
+struct AttnArgs {
+  const void* qkv;      // [L][3*H*128] bf16
+  void* O;              // [L][H*128] bf16
+  float* lse;           // [H][L] or nullptr
+  int L, H;
+  int causal;
+  float sm_scale;
+};
+
+cudaError_t launch_attention(const AttnArgs& a, const DevCtx& ctx, cudaStream_t st);
+
+cudaError_t launch_wait_selftest(const DevCtx& ctx, cudaStream_t st);
+
+}  // namespace h3

@@ -1,0 +1,49 @@
+"""Parity metrics shared by the GPU tests (test helper, no method arithmetic)."""
+import numpy as np
+
+# Tolerances of the block: max |err| <= 2e-2 * RMS(ref) and mean relative
+# error (ratio of L1 norms) <= 5e-3, bf16 storage with fp32 accumulation.
+MAX_REL_RMS = 2e-2
+MEAN_REL = 5e-3
+
+
+def to64(t) -> np.ndarray:
+    """A torch tensor (any device, any float dtype) widened to float64 numpy."""
+    return t.detach().float().cpu().double().numpy()
+
+
+# Unit roundoff of bf16 (8 significant bits): storing a value in bf16 moves
+# it by up to 2^-8 of itself.  A bf16-stored tensor with a heavy-tailed
+# magnitude distribution (an attention output O, where a few rows are single
+# values of V and most are averages) cannot meet max|err| <= 2e-2*RMS through
+# its own output rounding alone, so intermediates are checked element-wise
+# against 2e-2*RMS + 2^-8*|ref|; the block output keeps the plain bound.
+BF16_U = 2.0 ** -8
+
+
+def stats(got: np.ndarray, ref: np.ndarray):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape, (got.shape, ref.shape)
+    assert np.all(np.isfinite(got)), "non-finite values in the GPU output"
+    err = np.abs(got - ref)
+    rms = float(np.sqrt(np.mean(ref * ref)))
+    l1 = float(np.abs(ref).sum())
+    return float(err.max()) / max(rms, 1e-300), float(err.sum()) / max(l1, 1e-300)
+
+
+def assert_parity(got, ref, what: str, max_rel_rms: float = MAX_REL_RMS,
+                  mean_rel: float = MEAN_REL, bf16_storage: bool = True):
+    """Mean relative error <= mean_rel and, per element,
+    |err| <= max_rel_rms * RMS(ref) (+ 2^-8 |ref| when bf16_storage)."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    mx, mr = stats(got, ref)
+    rms = float(np.sqrt(np.mean(ref * ref)))
+    bound = max_rel_rms * rms + (BF16_U * np.abs(ref) if bf16_storage else 0.0)
+    excess = float(np.max(np.abs(got - ref) - bound))
+    assert excess <= 0.0 and mr <= mean_rel, (
+        f"{what}: max|err|/rms = {mx:.3e} (bound {max_rel_rms}"
+        f"{' + 2^-8|ref|' if bf16_storage else ''}, worst excess {excess:.3e}), "
+        f"mean rel = {mr:.3e} (<= {mean_rel})")
+    return mx, mr

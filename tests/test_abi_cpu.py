@@ -1,0 +1,135 @@
+"""The C-ABI library on a machine without a GPU: it builds, loads, exports
+every entry point include/h3attn.h declares, rejects bad arguments before
+launching anything, and its host-side packed layout equals the oracle's."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle as orc
+from h3inputs import CONFIGS
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from joint_audio_video_gb300 import build
+    build.build()
+    import joint_audio_video_gb300 as h3
+    return h3
+
+
+def _declared():
+    with open(os.path.join(ROOT, "include", "h3attn.h")) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"^\s*(?:const char\*|h3_status|void)\s+(h3_\w+)\s*\(", text, re.M)))
+
+
+def test_library_exports_every_declared_entry_point(lib):
+    names = _declared()
+    assert len(names) == 14, names
+    raw = ctypes.CDLL(lib.lib_path)
+    for n in names:
+        assert hasattr(raw, n), f"{n} declared but not exported"
+    assert sorted(lib.EXPORTED_SYMBOLS) == names
+    assert lib.h3_version().startswith("h3attn")
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        assert lib.h3_status_string(code)
+    assert lib.h3_status_string(99) == "unknown status"
+
+
+def _bad(fn, *args):
+    return fn(*args)
+
+
+def test_invalid_arguments_are_rejected_before_any_launch(lib):
+    L = lib.load()
+    p = 1 << 20          # an aligned fake address: never dereferenced on these paths
+    mis = p + 2          # misaligned
+    INV, UNS = 1, 2
+    # modulate: L < 1, d not a multiple of 128, null/misaligned pointers, n_mod range, eps
+    assert L.h3_adaln_modulate(p, p, p, p, 0, 256, 3, 1e-6, p, None) == INV
+    assert L.h3_adaln_modulate(p, p, p, p, 8, 200, 3, 1e-6, p, None) == INV
+    assert L.h3_adaln_modulate(p, p, p, p, 8, 32768, 3, 1e-6, p, None) == INV
+    assert L.h3_adaln_modulate(None, p, p, p, 8, 256, 3, 1e-6, p, None) == INV
+    assert L.h3_adaln_modulate(mis, p, p, p, 8, 256, 3, 1e-6, p, None) == INV
+    assert L.h3_adaln_modulate(p, p, p, p, 8, 256, 0, 1e-6, p, None) == INV
+    assert L.h3_adaln_modulate(p, p, p, p, 8, 256, 256, 1e-6, p, None) == INV
+    assert L.h3_adaln_modulate(p, p, p, p, 8, 256, 3, -1.0, p, None) == INV
+    assert L.h3_adaln_modulate(p, p, p, p, 8, 256, 3, float("nan"), p, None) == INV
+    # in-place y overlapping x partially
+    assert L.h3_adaln_modulate(p, p, p, p, 8, 256, 3, 1e-6, p + 16, None) == INV
+    # projection: overlap of y and qkv
+    assert L.h3_qkv_proj(p, p, 8, 256, p, None) == INV
+    assert L.h3_qkv_proj(p, p, 0, 256, p + (1 << 16), None) == INV
+    # rope: head_dim, sections, base
+    sec = (ctypes.c_int32 * 3)(32, 48, 48)
+    bad_sec = (ctypes.c_int32 * 3)(32, 47, 49)
+    short_sec = (ctypes.c_int32 * 3)(32, 48, 40)
+    assert L.h3_mrope_apply(p, p, 8, 2, 64, ctypes.addressof(sec), 1e4, None) == UNS
+    assert L.h3_mrope_apply(p, p, 8, 2, 128, ctypes.addressof(bad_sec), 1e4, None) == INV
+    assert L.h3_mrope_apply(p, p, 8, 2, 128, ctypes.addressof(short_sec), 1e4, None) == INV
+    assert L.h3_mrope_apply(p, p, 8, 2, 128, None, 1e4, None) == INV
+    assert L.h3_mrope_apply(p, p, 8, 2, 128, ctypes.addressof(sec), -1.0, None) == INV
+    # attention: head_dim, causal flag, scale, aliasing
+    assert L.h3_joint_attn_fwd(p, 8, 2, 64, 0, 0.1, p + (1 << 16), None, None) == UNS
+    assert L.h3_joint_attn_fwd(p, 8, 2, 128, 2, 0.1, p + (1 << 16), None, None) == INV
+    assert L.h3_joint_attn_fwd(p, 8, 2, 128, 0, 0.0, p + (1 << 16), None, None) == INV
+    assert L.h3_joint_attn_fwd(p, 8, 2, 128, 0, 0.1, p, None, None) == INV
+    assert L.h3_joint_attn_fwd(p, 8, 2, 128, 0, 0.1, p + (1 << 16), mis, None) == INV
+    # out projection: O aliasing out
+    assert L.h3_out_proj_gated_residual(p, p, p + (1 << 16), p, p, 8, 256, 3, p, None) == INV
+    assert L.h3_out_proj_gated_residual(p, p, p, p, p, 8, 256, 0, p + (1 << 16), None) == INV
+
+
+def test_block_descriptor_and_workspace(lib):
+    desc = lib.BlockDesc.make(L=58758, d=5120, n_heads=40)
+    n = lib.h3_workspace_size(desc)
+    L, d = 58758, 5120
+    r = lambda x: (x + 255) // 256 * 256
+    assert n == r(L * d * 2) + r(L * 3 * d * 2)
+    for bad in (dict(L=0), dict(d=5000), dict(n_heads=39), dict(rope_sec=(32, 48, 50)),
+                dict(ln_eps=-1.0), dict(n_mod=0), dict(rope_base=0.0)):
+        kw = dict(L=64, d=256, n_heads=2)
+        kw.update(bad)
+        with pytest.raises(lib.H3Error) as e:
+            lib.h3_workspace_size(lib.BlockDesc.make(**kw))
+        assert e.value.status == 1
+    with pytest.raises(lib.H3Error) as e:
+        lib.h3_workspace_size(lib.BlockDesc.make(L=64, d=512, n_heads=8, head_dim=64))
+    assert e.value.status == 2
+    # a workspace that is too small is refused before launch
+    desc = lib.BlockDesc.make(L=64, d=256, n_heads=2)
+    need = lib.h3_workspace_size(desc)
+    p = 1 << 24
+    with pytest.raises(lib.H3Error) as e:
+        lib.h3_attn_block_fwd(desc, p, p, p, p, p, p, p, p, 1 << 30, need - 1, p + (1 << 20),
+                              stream=0)
+    assert e.value.status == 6
+
+
+@pytest.mark.parametrize("name", sorted(CONFIGS))
+def test_host_layout_equals_oracle_bit_exact(lib, name):
+    c = CONFIGS[name]
+    args = (c.n_text, c.video_t, c.video_h, c.video_w, c.audio_channels, c.audio_steps)
+    mod, pos = lib.h3_build_packed_layout(*args)
+    omod, opos = orc.packed_layout(*args)
+    assert mod.dtype == np.uint8 and pos.dtype == np.int32
+    assert np.array_equal(mod, omod) and np.array_equal(pos, opos)
+
+
+def test_host_layout_rejects_bad_counts(lib):
+    with pytest.raises(lib.H3Error):
+        lib.h3_build_packed_layout(0, 0, 0, 0, 0, 0)
+    with pytest.raises(lib.H3Error):
+        lib.h3_build_packed_layout(-1, 2, 2, 2, 2, 2)
+    L = lib.load()
+    mod = np.zeros(4, np.uint8)
+    pos = np.zeros((4, 3), np.int32)
+    assert L.h3_build_packed_layout(3, 1, 1, 2, 0, 0, mod.ctypes.data, pos.ctypes.data, 4) == 1
