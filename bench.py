@@ -106,9 +106,9 @@ def oracle_sample(cfg, inp, scale_factor: float = 1.0):
     from h3inputs import attention_qkv
 
     L, d, H = cfg.L, cfg.d, cfg.n_heads
-    R1 = int(4096 * scale_factor)
-    R2 = int(384 * scale_factor)
-    R3, H3 = int(128 * scale_factor), 4
+    R1 = min(L, int(4096 * scale_factor))
+    R2 = min(L, int(384 * scale_factor))
+    R3, H3 = min(L, int(128 * scale_factor)), 4
     f64 = lambda t: t.float().double().numpy()
     mod, pos = orc.packed_layout(cfg.n_text, cfg.video_t, cfg.video_h, cfg.video_w,
                                  cfg.audio_channels, cfg.audio_steps)
@@ -329,7 +329,7 @@ def run_gpu(args, cfg):
         "wall_s_timed": wall,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        full, sample, cores, _ = oracle_sample(cfg, inp, scale_factor=8.0)
+        full, sample, cores, _ = oracle_sample(cfg, inp, scale_factor=24.0)
         line["cpu_baseline"] = {"value": flops / full / 1e12, "unit": UNIT, "cores": cores,
                                 "kind": "oracle", "sample": sample,
                                 "extrapolated_block_s": full}
@@ -345,7 +345,7 @@ def main():
     ap = argparse.ArgumentParser(description=__doc__,
                                  formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="h3", choices=["h3", "reference"])
     ap.add_argument("--config", default="full", help="block workload (default: full, L=58758)")

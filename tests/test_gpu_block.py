@@ -18,6 +18,7 @@ from tests._parity import assert_parity, to64
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
+CHAIN_MAX_REL_RMS = 4e-2
 
 
 def _layouts(h3, c):
@@ -58,7 +59,9 @@ def test_block_parity_full_rows(h3, name, causal):
     r = orc.block(o["x"], omod, opos, o["shift"], o["scale"], o["gate"], o["Wqkv"], o["Wo"],
                   c.n_heads, causal=causal)
     assert_parity(to64(qkv), r["qkv"], f"{name} qkv (rotated)")
-    assert_parity(to64(O), r["O"], f"{name} O")
+    # O inside the chain also carries the bf16 storage of y and of the rotated
+    # q, k (each logit moves by ~2^-8 against the fp64 chain): twice the bound
+    assert_parity(to64(O), r["O"], f"{name} O", max_rel_rms=CHAIN_MAX_REL_RMS)
     assert_parity(to64(out), r["out"], f"{name} out", bf16_storage=False)
     # the branch O Wo^T on its own (the residual dilutes its errors in out):
     # the output projection with a zero residual and a unit gate
@@ -68,7 +71,8 @@ def test_block_parity_full_rows(h3, name, causal):
                                   torch.zeros(L, dtype=torch.uint8, device=DEV),
                                   torch.ones(1, d, device=DEV), L, d, 1, br)
     assert h3.h3_sync_status() == 0
-    assert_parity(to64(br), r["branch"], f"{name} branch O Wo^T")
+    assert_parity(to64(br), r["branch"], f"{name} branch O Wo^T",
+                  max_rel_rms=CHAIN_MAX_REL_RMS)
 
 
 def test_block_separate_calls_match_oracle(h3):
@@ -93,7 +97,7 @@ def test_block_separate_calls_match_oracle(h3):
     r = orc.block(o["x"], omod, opos, o["shift"], o["scale"], o["gate"], o["Wqkv"], o["Wo"], H)
     assert_parity(to64(y), r["y"], "y")
     assert_parity(to64(qkv), r["qkv"], "qkv")
-    assert_parity(to64(O), r["O"], "O")
+    assert_parity(to64(O), r["O"], "O", max_rel_rms=CHAIN_MAX_REL_RMS)
     assert_parity(to64(out), r["out"], "out", bf16_storage=False)
 
 
@@ -111,7 +115,8 @@ def test_block_parity_medium_sampled_rows(h3, causal):
     q = to64(qkv[torch.from_numpy(rows).to(DEV)])
     assert_parity(q[:, :d], r["q"], "medium q rows")
     assert_parity(to64(qkv[:, d:2 * d]), r["k"], "medium k (all rows)")
-    assert_parity(to64(O[torch.from_numpy(rows).to(DEV)]), r["O"], "medium O rows")
+    assert_parity(to64(O[torch.from_numpy(rows).to(DEV)]), r["O"], "medium O rows",
+                  max_rel_rms=CHAIN_MAX_REL_RMS)
     assert_parity(to64(out[torch.from_numpy(rows).to(DEV)]), r["out"], "medium out rows",
                   bf16_storage=False)
 
