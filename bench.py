@@ -35,6 +35,12 @@ UNIT = "TFLOP/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
+def _workload(cfg) -> str:
+    return (f"joint A/V DiT attention sub-block, L={cfg.L} ({cfg.n_text} text + {cfg.n_video} "
+            f"video + {cfg.n_audio} audio), d={cfg.d}, {cfg.n_heads}x{cfg.head_dim} heads, "
+            f"full attention, batch 1")
+
+
 def _peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -163,9 +169,7 @@ def run_reference(args, cfg):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": full * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "joint A/V DiT attention sub-block, L=58758 (358 text + "
-                               "57600 video + 800 audio), d=5120, 40x128 heads, full attention",
-                   "L": cfg.L, "d": cfg.d, "heads": cfg.n_heads},
+        "config": {"workload": _workload(cfg), "L": cfg.L, "d": cfg.d, "heads": cfg.n_heads},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -309,11 +313,10 @@ def run_gpu(args, cfg):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": "joint A/V DiT attention sub-block, L=58758 (358 text + 57600 "
-                               "video + 800 audio), d=5120, 40x128 heads, full attention, "
-                               "batch 1",
+        "config": {"workload": _workload(cfg),
                    "L": L, "d": d, "heads": H, "causal": False,
-                   "l2": "inputs larger than L2 (x 602 MB, qkv 1.8 GB per step)",
+                   "l2": f"inputs larger than L2 (x {L * d * 2 / 1e6:.0f} MB, qkv "
+                         f"{L * 3 * d * 2 / 1e9:.2f} GB per step)",
                    "parallelism": f"replicas x{world}"},
         "tokens_per_s": world * L / (ms * 1e-3),
         "pct_of_bf16_peak_block": flops / (ms * 1e-3) / 1e12 / peak,
