@@ -192,6 +192,35 @@ h3_status h3_attn_block_fwd_profiled(const h3_block_desc* desc, const uint16_t* 
                                      const uint16_t* Wo, void* workspace, size_t workspace_bytes,
                                      uint16_t* out, h3_stream_t stream, void* const* events);
 
+/* Size of the workspace that h3_attn_block_fwd_noalloc keeps on every GPU: 64 MiB. */
+#define H3_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+
+/*
+ * h3_attn_block_fwd for callers that cannot allocate device memory (the pages
+ * have no counterpart: this is an interface convenience, not part of the
+ * method).  An engine that plans every device buffer before it runs and hands
+ * its plugins only their inputs and outputs, or a process whose caching
+ * allocator already holds the GPU's memory, cannot get a workspace from
+ * cudaMalloc at call time.  This call uses instead a workspace the library
+ * keeps in device global memory: H3_NOALLOC_SCRATCH_BYTES per GPU that loads
+ * the library, held until the process exits.  It calls no cudaMalloc,
+ * cudaFree or other allocating routine.
+ *   - Arguments as in h3_attn_block_fwd, without workspace and size.
+ *   - Returns H3_ERR_WORKSPACE, launching nothing, when h3_workspace_size(desc)
+ *     exceeds H3_NOALLOC_SCRATCH_BYTES (e.g. 4,096 tokens at d = 2048 fit
+ *     exactly; 58,758 tokens at d = 5120 do not).
+ *   - The first call on a device looks up the workspace's device address
+ *     (cudaGetSymbolAddress) with that device current: make it before any
+ *     stream capture begins.
+ *   - All calls on a device share the one workspace and it keeps the last
+ *     call's contents (nothing in it needs to start at zero).  Calls that
+ *     overlap on the GPU race on it: order them on one stream or with events.
+ */
+h3_status h3_attn_block_fwd_noalloc(const h3_block_desc* desc, const uint16_t* x,
+                                    const uint8_t* mod, const int32_t* pos, const float* shift,
+                                    const float* scale, const float* gate, const uint16_t* Wqkv,
+                                    const uint16_t* Wo, uint16_t* out, h3_stream_t stream);
+
 /*
  * Synchronise `stream`, then report and clear the current device's status
  * word: H3_OK, H3_ERR_TIMEOUT, H3_ERR_BAD_INDEX or H3_ERR_CUDA.

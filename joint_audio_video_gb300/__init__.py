@@ -20,7 +20,8 @@ __all__ = [
     "h3_build_packed_layout", "h3_adaln_modulate", "h3_qkv_proj", "h3_mrope_apply",
     "h3_joint_attn_fwd", "h3_out_proj_gated_residual", "h3_workspace_size",
     "h3_attn_block_fwd", "h3_sync_status", "h3_set_wait_limit_ns",
-    "h3_selftest_wait_timeout", "h3_attn_block_fwd_profiled", "EXPORTED_SYMBOLS",
+    "h3_selftest_wait_timeout", "h3_attn_block_fwd_profiled", "h3_attn_block_fwd_noalloc",
+    "NOALLOC_SCRATCH_BYTES", "EXPORTED_SYMBOLS",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -34,8 +35,11 @@ EXPORTED_SYMBOLS = (
     "h3_status_string", "h3_version", "h3_build_packed_layout", "h3_adaln_modulate",
     "h3_qkv_proj", "h3_mrope_apply", "h3_joint_attn_fwd", "h3_out_proj_gated_residual",
     "h3_workspace_size", "h3_attn_block_fwd", "h3_sync_status", "h3_set_wait_limit_ns",
-    "h3_selftest_wait_timeout", "h3_attn_block_fwd_profiled",
+    "h3_selftest_wait_timeout", "h3_attn_block_fwd_profiled", "h3_attn_block_fwd_noalloc",
 )
+
+# Workspace the library keeps per GPU for h3_attn_block_fwd_noalloc.
+NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
 class H3Error(RuntimeError):
@@ -79,6 +83,7 @@ def _sig(lib):
                                                                                   _P, _P]
     lib.h3_attn_block_fwd_profiled.argtypes = (
         [ctypes.POINTER(BlockDesc)] + [_P] * 9 + [ctypes.c_size_t, _P, _P, _P])
+    lib.h3_attn_block_fwd_noalloc.argtypes = [ctypes.POINTER(BlockDesc)] + [_P] * 10
     lib.h3_sync_status.argtypes = [_P]
     lib.h3_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
     lib.h3_set_wait_limit_ns.restype = None
@@ -212,6 +217,15 @@ def h3_attn_block_fwd_profiled(desc: BlockDesc, x, mod, pos, shift, scale, gate,
         ctypes.byref(desc), _addr(x), _addr(mod), _addr(pos), _addr(shift), _addr(scale),
         _addr(gate), _addr(Wqkv), _addr(Wo), _addr(workspace), int(workspace_bytes), _addr(out),
         _stream(stream), arr))
+
+
+def h3_attn_block_fwd_noalloc(desc: BlockDesc, x, mod, pos, shift, scale, gate, Wqkv, Wo, out,
+                              stream=None) -> None:
+    """The fused block on the library's own per-GPU workspace (no allocation
+    anywhere); for shapes whose workspace fits NOALLOC_SCRATCH_BYTES."""
+    _check("h3_attn_block_fwd_noalloc", load().h3_attn_block_fwd_noalloc(
+        ctypes.byref(desc), _addr(x), _addr(mod), _addr(pos), _addr(shift), _addr(scale),
+        _addr(gate), _addr(Wqkv), _addr(Wo), _addr(out), _stream(stream)))
 
 
 def h3_sync_status(stream=None) -> int:
