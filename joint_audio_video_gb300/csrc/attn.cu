@@ -56,6 +56,50 @@ __device__ __forceinline__ float ex2(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+// Packed pairs of fp32 in one 64-bit register (low word = first value).
+__device__ __forceinline__ uint64_t f2(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void unf2(uint64_t v, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// Maximum of 32 raw scores as a chain of 16 three-input max operations.
+__device__ __forceinline__ float max32(const uint32_t (&r)[32]) {
+  float m = max3(__uint_as_float(r[0]), __uint_as_float(r[1]), __uint_as_float(r[2]));
+#pragma unroll
+  for (int i = 3; i < 31; i += 2) m = max3(m, __uint_as_float(r[i]), __uint_as_float(r[i + 1]));
+  return fmaxf(m, __uint_as_float(r[31]));
+}
+// p = 2^(s*c - m) for 32 raw scores: 16 bf16 pairs into pk, row sum into acc.
+__device__ __forceinline__ void exp32(const uint32_t (&r)[32], uint64_t cc, uint64_t nm,
+                                      uint32_t* pk, uint64_t (&acc)[2]) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    float a, b;
+    unf2(ffma2(f2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), cc, nm), a, b);
+    a = ex2(a);
+    b = ex2(b);
+    acc[i & 1] = fadd2(acc[i & 1], f2(a, b));
+    pk[i] = pack_bf16x2(a, b);
+  }
+}
 
 __device__ __forceinline__ void s_product(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem) {
   constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 0, 0);
@@ -77,6 +121,9 @@ __device__ __forceinline__ void pv_product(uint32_t o_tmem, uint32_t p_tmem, uin
   }
 }
 
+// Registers are split over the SM's four sub-partitions (16K each) and warp w
+// runs on sub-partition w % 4, so with 10 warps three share one sub-partition:
+// at most 168 registers per thread.
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm, const __grid_constant__ AttnDev p) {
   extern __shared__ uint8_t smem_raw[];
@@ -253,26 +300,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld_wait(r1);
       tmem_ld_wait(r2);
       tmem_ld_wait(r3);
-      float s[128];
-#pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        s[c] = __uint_as_float(r0[c]) * p.scale_log2;
-        s[32 + c] = __uint_as_float(r1[c]) * p.scale_log2;
-        s[64 + c] = __uint_as_float(r2[c]) * p.scale_log2;
-        s[96 + c] = __uint_as_float(r3[c]) * p.scale_log2;
-      }
       const int kv0 = j * 128;
       const bool tail = kv0 + 128 > p.L;
       const bool diag = p.causal && kv0 + 127 > tile_q0;
       if (tail || diag) {
-        const int lim = p.causal ? min(p.L - 1, qi) : p.L - 1;   // last visible key
+        const int lim = (p.causal ? min(p.L - 1, qi) : p.L - 1) - kv0;   // last visible key
+        constexpr uint32_t kNegInf = 0xFF800000u;
 #pragma unroll
-        for (int c = 0; c < 128; ++c)
-          if (kv0 + c > lim) s[c] = -INFINITY;
+        for (int c = 0; c < 32; ++c) {
+          if (c > lim) r0[c] = kNegInf;
+          if (c + 32 > lim) r1[c] = kNegInf;
+          if (c + 64 > lim) r2[c] = kNegInf;
+          if (c + 96 > lim) r3[c] = kNegInf;
+        }
       }
-      float mx = s[0];
-#pragma unroll
-      for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
+      // row maximum of the raw scores (scale > 0 commutes with max)
+      const float mx = fmaxf(max3(max32(r0), max32(r1), max32(r2)), max32(r3)) * p.scale_log2;
       if (j == 0) {
         m_used = mx;
       } else {
@@ -294,23 +337,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (need) m_used = m_new;
         }
       }
+      // p = 2^(s * scale_log2 - m_used), rounded to bf16 pairs over S's first 64 columns
+      const uint64_t cc = f2(p.scale_log2, p.scale_log2), nm = f2(-m_used, -m_used);
+      uint64_t acc[2] = {0ull, 0ull};
       uint32_t pk0[32], pk1[32];
-      float sum = 0.f;
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const float a = ex2(s[2 * i] - m_used), b = ex2(s[2 * i + 1] - m_used);
-        sum += a + b;
-        pk0[i] = pack_bf16x2(a, b);
-      }
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const float a = ex2(s[64 + 2 * i] - m_used), b = ex2(s[64 + 2 * i + 1] - m_used);
-        sum += a + b;
-        pk1[i] = pack_bf16x2(a, b);
-      }
-      l += sum;
+      exp32(r0, cc, nm, pk0, acc);
+      exp32(r1, cc, nm, pk0 + 16, acc);
       tmem_st32(tS, pk0);
+      exp32(r2, cc, nm, pk1, acc);
+      exp32(r3, cc, nm, pk1 + 16, acc);
       tmem_st32(tS + 32, pk1);
+      float a0, a1, b0, b1;
+      unf2(acc[0], a0, a1);
+      unf2(acc[1], b0, b1);
+      l += (a0 + a1) + (b0 + b1);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bp);
