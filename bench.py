@@ -304,9 +304,14 @@ def run_gpu(args, cfg):
     achieved = attn_flops / (per["attention"] * 1e-3) / 1e12
     traffic = None
     tf = os.path.join(ROOT, "profiles", "attention_traffic.json")
-    if os.path.exists(tf):
+    if os.path.exists(tf) and cfg.name == "full":
+        import hashlib
         with open(tf) as f:
-            traffic = json.load(f).get("bytes_per_launch_full")
+            rec = json.load(f)
+        with open(os.path.join(ROOT, rec["source"]), "rb") as f:
+            same = hashlib.sha256(f.read()).hexdigest() == rec.get("source_sha256")
+        # counters taken on another version of the kernel do not describe this one
+        traffic = rec.get("bytes_per_launch_full") if same else None
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
