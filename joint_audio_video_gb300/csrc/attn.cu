@@ -101,24 +101,26 @@ __device__ __forceinline__ void exp32(const uint32_t (&r)[32], uint64_t cc, uint
   }
 }
 
-__device__ __forceinline__ void s_product(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem) {
+// The MMA issuer keeps every operand descriptor precomputed: issuing one
+// 128x128x16 MMA (64 tensor-core cycles) must cost far less than 64 cycles
+// of the issuing thread, or the tensor core waits on the issuer.
+// S = Q K^T: both K-major, 8 steps of K=16 over the two 64-column boxes.
+__device__ __forceinline__ void s_product(uint32_t d_tmem, SDesc q, SDesc k) {
   constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 0, 0);
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    const uint32_t off = (k >> 2) * kBox + (k & 3) * 32;
-    mma_bf16_ss(d_tmem, sdesc_sw128(q_smem + off, 16, 1024), sdesc_sw128(k_smem + off, 16, 1024),
-                idesc, k > 0);
+  for (int s = 0; s < 8; ++s) {
+    const uint32_t off = (s >> 2) * kBox + (s & 3) * 32;
+    mma_bf16_ss(d_tmem, sdesc_at(q, off), sdesc_at(k, off), idesc, s > 0);
   }
 }
 
-__device__ __forceinline__ void pv_product(uint32_t o_tmem, uint32_t p_tmem, uint32_t v_smem,
+// O += P V: P (bf16 pairs) from TMEM, V as the MN-major operand, 8 steps of 16 keys.
+__device__ __forceinline__ void pv_product(uint32_t o_tmem, uint32_t p_tmem, SDesc v,
                                            bool accumulate) {
   constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 0, 1);
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    mma_bf16_ts(o_tmem, p_tmem + k * 8, sdesc_sw128(v_smem + k * 2048, kBox, 1024), idesc,
-                accumulate || k > 0);
-  }
+  for (int s = 0; s < 8; ++s)
+    mma_bf16_ts(o_tmem, p_tmem + s * 8, sdesc_at(v, s * 2048), idesc, accumulate || s > 0);
 }
 
 // Registers are split over the SM's four sub-partitions (16K each) and warp w
@@ -211,8 +213,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane_id() == 0) {
       bool ok = mbar_wait(smem_u32(&bar_q), 0, wc);
+      // descriptors of Q0, Q1 and of every ring slot read as K (K-major) or V (MN-major)
+      const SDesc dQ0 = sdesc_split(sdesc_sw128(sQ, 16, 1024));
+      const SDesc dQ1 = sdesc_split(sdesc_sw128(sQ + kTile, 16, 1024));
+      // slots are kTile apart: a slot's descriptor is the first slot's plus s * kTile / 16
+      const SDesc dK0 = sdesc_split(sdesc_sw128(sRing, 16, 1024));
+      const SDesc dV0 = sdesc_split(sdesc_sw128(sRing, kBox, 1024));
+      auto dK = [&](uint32_t slot_idx) { return SDesc{dK0.lo + slot_idx * (kTile >> 4), dK0.hi}; };
+      auto dV = [&](uint32_t slot_idx) { return SDesc{dV0.lo + slot_idx * (kTile >> 4), dV0.hi}; };
       auto slot = [&](int r, uint32_t& addr, uint32_t& par) {
-        addr = sRing + (r % kStages) * kTile;
+        addr = uint32_t(r % kStages);
         par = (r / kStages) & 1;
       };
       auto kv_full = [&](int r) { return smem_u32(&bar_kv_full[r % kStages]); };
@@ -225,9 +235,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (ok) {
         tc_fence_after();
-        s_product(tS0, sQ, kA);
+        s_product(tS0, dQ0, dK(kA));
         tc_commit(smem_u32(&bar_s[0]));
-        s_product(tS1, sQ + kTile, kA);
+        s_product(tS1, dQ1, dK(kA));
         tc_commit(smem_u32(&bar_s[1]));
         tc_commit(kv_empty(0));
       }
@@ -239,15 +249,15 @@ __global__ void __launch_bounds__(kThreads, 1)
              mbar_wait(smem_u32(&bar_p[0]), pph, wc);
         if (!ok) break;
         tc_fence_after();
-        pv_product(tO0, tS0, vA, j > 1);
-        s_product(tS0, sQ, kA);
+        pv_product(tO0, tS0, dV(vA), j > 1);
+        s_product(tS0, dQ0, dK(kA));
         tc_commit(smem_u32(&bar_s[0]));
         ok = mbar_wait(smem_u32(&bar_p[1]), pph, wc);
         if (!ok) break;
         tc_fence_after();
-        pv_product(tO1, tS1, vA, j > 1);
+        pv_product(tO1, tS1, dV(vA), j > 1);
         tc_commit(kv_empty(2 * j - 1));
-        s_product(tS1, sQ + kTile, kA);
+        s_product(tS1, dQ1, dK(kA));
         tc_commit(smem_u32(&bar_s[1]));
         tc_commit(kv_empty(2 * j));
       }
@@ -258,12 +268,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = mbar_wait(kv_full(2 * j - 1), vP, wc) && mbar_wait(smem_u32(&bar_p[0]), pph, wc);
         if (ok) {
           tc_fence_after();
-          pv_product(tO0, tS0, vA, j > 1);
+          pv_product(tO0, tS0, dV(vA), j > 1);
           ok = mbar_wait(smem_u32(&bar_p[1]), pph, wc);
         }
         if (ok) {
           tc_fence_after();
-          pv_product(tO1, tS1, vA, j > 1);
+          pv_product(tO1, tS1, dV(vA), j > 1);
           tc_commit(kv_empty(2 * j - 1));
           tc_commit(smem_u32(&bar_o));
         }

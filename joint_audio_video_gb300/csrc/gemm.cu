@@ -198,6 +198,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------------- MMA issuer
     if (lane_id() == 0) {
       constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, 0, 0);
+      // stages are kStageBytes apart: precomputed descriptors plus one add per MMA
+      const SDesc dA0 = sdesc_split(sdesc_sw128(base, 16, 1024));
+      const SDesc dB0 = sdesc_split(sdesc_sw128(base + Cfg::kABytes, 16, 1024));
       int stage = 0;
       uint32_t phase = 0;
       int it = 0;
@@ -211,13 +214,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!mbar_wait(smem_u32(&bar_full[stage]), phase, wc)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t sa = base + stage * Cfg::kStageBytes;
-          const uint32_t sb = sa + Cfg::kABytes;
+          const uint32_t soff = stage * (Cfg::kStageBytes >> 4);
+          const SDesc dA{dA0.lo + soff, dA0.hi}, dB{dB0.lo + soff, dB0.hi};
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k) {
-            mma_bf16_ss(dtm, sdesc_sw128(sa + k * 32, 16, 1024), sdesc_sw128(sb + k * 32, 16, 1024),
-                        idesc, (kb | k) != 0);
-          }
+          for (int k = 0; k < BK / 16; ++k)
+            mma_bf16_ss(dtm, sdesc_at(dA, k * 32), sdesc_at(dB, k * 32), idesc, (kb | k) != 0);
           tc_commit(smem_u32(&bar_empty[stage]));
           if (++stage == S) { stage = 0; phase ^= 1u; }
         }

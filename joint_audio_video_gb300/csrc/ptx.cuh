@@ -180,6 +180,22 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   return d;
 }
 
+// A descriptor split into its two 32-bit words, so the start address of a
+// sub-tile is one 32-bit add (start >> 4 lives in the low 14 bits and every
+// shared-memory address of the CTA fits them without carry).
+struct SDesc {
+  uint32_t lo, hi;
+};
+__device__ __forceinline__ SDesc sdesc_split(uint64_t d) {
+  return SDesc{uint32_t(d), uint32_t(d >> 32)};
+}
+// Descriptor of the sub-tile `byte_off` bytes after the described start.
+__device__ __forceinline__ uint64_t sdesc_at(SDesc d, uint32_t byte_off) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(d.lo + (byte_off >> 4)), "r"(d.hi));
+  return r;
+}
+
 // ---- tensor memory <-> registers (32 lanes x 32 bit, one row per thread)
 #define H3_R8(i) "=r"(r[i]), "=r"(r[i + 1]), "=r"(r[i + 2]), "=r"(r[i + 3]), \
                  "=r"(r[i + 4]), "=r"(r[i + 5]), "=r"(r[i + 6]), "=r"(r[i + 7])
