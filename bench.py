@@ -261,31 +261,58 @@ def run_gpu(args, cfg):
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         ms = float(tt.item())
 
-    # ---- end to end through the public API with host buffers
+    # ---- end to end through the public API with host buffers: every step uploads
+    # its input x and modulation vectors from pinned host memory and downloads its
+    # output.  Copies run on a second stream, double-buffered, so step k's
+    # compute overlaps step k+1's upload and step k-1's download.
     x_host = inp["x"].pin_memory()
     mod_host = {k: inp[k].pin_memory() for k in ("shift", "scale", "gate")}
-    out_host = torch.empty(L, d, dtype=torch.bfloat16).pin_memory()
+    out_host = [torch.empty(L, d, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
     h2d = x_host.numel() * 2 + sum(v.numel() * 4 for v in mod_host.values())
-    d2h = out_host.numel() * 2
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    d2h = out_host[0].numel() * 2
+    xb = [x, torch.empty_like(x)]
+    ob = [out, torch.empty_like(out)]
+    mb = [{k: v for k, v in (("shift", shift), ("scale", scale), ("gate", gate))},
+          {k: torch.empty_like(v) for k, v in (("shift", shift), ("scale", scale), ("gate", gate))}]
+    cs = torch.cuda.Stream(dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_done = [torch.cuda.Event() for _ in range(2)]
 
-    def e2e_step():
-        x.copy_(x_host, non_blocking=True)
-        shift.copy_(mod_host["shift"], non_blocking=True)
-        scale.copy_(mod_host["scale"], non_blocking=True)
-        gate.copy_(mod_host["gate"], non_blocking=True)
-        h3.h3_attn_block_fwd(desc, x, mod_d, pos_d, shift, scale, gate, wqkv, wo, ws, nbytes,
-                             out, stream=stream)
-        out_host.copy_(out, non_blocking=True)
+    def upload(b):
+        with torch.cuda.stream(cs):
+            xb[b].copy_(x_host, non_blocking=True)
+            for k in ("shift", "scale", "gate"):
+                mb[b][k].copy_(mod_host[k], non_blocking=True)
+            ev_in[b].record(cs)
 
-    for _ in range(max(1, min(args.warmup, 2))):
-        e2e_step()
+    def download(b, k):
+        with torch.cuda.stream(cs):
+            cs.wait_event(ev_done[b])
+            out_host[k % 2].copy_(ob[b], non_blocking=True)
+
+    def e2e_run(n):
+        upload(0)
+        for k in range(n):
+            b = k % 2
+            stream.wait_event(ev_in[b])
+            h3.h3_attn_block_fwd(desc, xb[b], mod_d, pos_d, mb[b]["shift"], mb[b]["scale"],
+                                 mb[b]["gate"], wqkv, wo, ws, nbytes, ob[b], stream=stream)
+            ev_done[b].record(stream)
+            if k >= 1:
+                download(1 - b, k - 1)
+            if k + 1 < n:
+                if k >= 1:
+                    cs.wait_event(ev_done[1 - b])   # step k-1 no longer reads xb[1-b]
+                upload(1 - b)
+        download((n - 1) % 2, n - 1)
+
+    e2e_run(2)
     torch.cuda.synchronize(dev)
     barrier()
-    e0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
-    e1.record(stream)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(cs)
+    e2e_run(args.steps)
+    e1.record(cs)
     torch.cuda.synchronize(dev)
     e2e_ms = e0.elapsed_time(e1) / args.steps
     if world > 1:
@@ -295,6 +322,29 @@ def run_gpu(args, cfg):
     st = h3.h3_sync_status(stream)
     if st != 0:
         raise RuntimeError(f"device status after e2e steps: {h3.h3_status_string(st)}")
+
+    # ---- the 50-step denoising sweep: step k uses its own seeded modulation set
+    # and the previous step's output (in place) as its input
+    from h3inputs import sweep_modulation
+    sweep_mods = [{k: v.to(dev) for k, v in sweep_modulation(cfg, s).items()}
+                  for s in range(1, 51)]
+    xs = x.clone()
+    sev = [torch.cuda.Event(enable_timing=True) for _ in range(51)]
+    torch.cuda.synchronize(dev)
+    barrier()
+    sev[0].record(stream)
+    for s_i in range(50):
+        m = sweep_mods[s_i]
+        h3.h3_attn_block_fwd(desc, xs, mod_d, pos_d, m["shift"], m["scale"], m["gate"], wqkv, wo,
+                             ws, nbytes, xs, stream=stream)
+        sev[s_i + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    st = h3.h3_sync_status(stream)
+    if st != 0:
+        raise RuntimeError(f"device status after the sweep: {h3.h3_status_string(st)}")
+    sweep_steps = [sev[i].elapsed_time(sev[i + 1]) for i in range(50)]
+    sweep_total = sev[0].elapsed_time(sev[50])
+    del xs
 
     flops = cfg.flops()
     value = world * flops / (ms * 1e-3) / 1e12
@@ -332,6 +382,12 @@ def run_gpu(args, cfg):
                      "peak_kind": f"{peak_kind} bf16 sustained (kernel inside a long step)"},
         "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "sweep50": {"steps": 50, "total_ms": sweep_total,
+                    "per_step_ms": {"median": statistics.median(sweep_steps),
+                                    "min": min(sweep_steps), "max": max(sweep_steps)},
+                    "sustained_tflops": 50 * flops / (sweep_total * 1e-3) / 1e12,
+                    "frac_of_sustained_bf16_peak":
+                        50 * flops / (sweep_total * 1e-3) / 1e12 / peak},
         "gpu_launches": 4 * args.steps,
         "clocks": clocks,
         "wall_s_timed": wall,
