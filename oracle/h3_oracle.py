@@ -188,6 +188,35 @@ def attention(qkv: np.ndarray, n_heads: int, head_dim: int = 128,
     return out, lse
 
 
+def attention_varlen(qkv: np.ndarray, cu_seqlens, n_heads: int, head_dim: int = 128,
+                     causal: bool = False, sm_scale: Optional[float] = None,
+                     rows: Optional[np.ndarray] = None) -> Tuple[np.ndarray, np.ndarray]:
+    """Attention restricted to sub-sequences ([vLLM] §3, cu_seqlens and masks).
+
+    ``cu_seqlens = [0, c1, ..., L]`` cuts the packed sequence into segments
+    [c_s, c_{s+1}); a token attends only to keys of its own segment (and, when
+    causal, to those at or before it).  This is attention applied to each
+    segment's rows on their own.  Returns ``O [R, H*dh]`` and ``lse [H, R]``.
+    """
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    L = qkv.shape[0]
+    assert cu[0] == 0 and cu[-1] == L and np.all(np.diff(cu) >= 0)
+    if rows is None:
+        rows = np.arange(L, dtype=np.int64)
+    rows = np.asarray(rows, dtype=np.int64)
+    d = n_heads * head_dim
+    out = np.zeros((rows.shape[0], d), dtype=np.float64)
+    lse = np.zeros((n_heads, rows.shape[0]), dtype=np.float64)
+    seg = np.searchsorted(cu, rows, side="right") - 1
+    for s in np.unique(seg):
+        lo, hi = int(cu[s]), int(cu[s + 1])
+        pick = np.nonzero(seg == s)[0]
+        o, l = attention(qkv[lo:hi], n_heads, head_dim, causal, sm_scale, rows=rows[pick] - lo)
+        out[pick] = o
+        lse[:, pick] = l
+    return out, lse
+
+
 # ---------------------------------------------------------------------------
 # a6: gated residual ([H3-RL] modality-specific AdaLN branches: the gate)
 # ---------------------------------------------------------------------------

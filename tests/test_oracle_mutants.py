@@ -73,6 +73,26 @@ def _attention_causal_strict(qkv, n_heads, head_dim=128, causal=False, sm_scale=
     return out, lse
 
 
+def _varlen_boundary_off_by_one(qkv, cu_seqlens, n_heads, head_dim=128, causal=False,
+                                sm_scale=None, rows=None):
+    """A token on a segment start is put in the previous segment."""
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    L = qkv.shape[0]
+    rows = np.arange(L) if rows is None else np.asarray(rows)
+    d = n_heads * head_dim
+    out = np.zeros((len(rows), d))
+    lse = np.zeros((n_heads, len(rows)))
+    seg = np.maximum(np.searchsorted(cu, rows, side="left") - 1, 0)
+    for r, (i, s) in enumerate(zip(rows, seg)):
+        lo, hi = int(cu[s]), int(cu[s + 1])
+        if i >= hi:
+            lo, hi = lo, i + 1
+        o, l = _ORIG["attention"](qkv[lo:hi], n_heads, head_dim, causal, sm_scale,
+                                  rows=np.array([i - lo]))
+        out[r], lse[:, r] = o[0], l[:, 0]
+    return out, lse
+
+
 def _residual_wrong_index(x, branch, mod, gate):
     return x + gate[(mod.astype(np.int64) + 1) % 3] * branch
 
@@ -90,7 +110,7 @@ def _layout_audio_step_major(n_text, vt, vh, vw, ac, steps):
 
 _ORIG = {name: getattr(core, name) for name in
          ("layer_norm", "adaln_modulate", "linear", "rope_rotate_heads",
-          "rope_angles", "attention", "gated_residual", "packed_layout")}
+          "rope_angles", "attention", "attention_varlen", "gated_residual", "packed_layout")}
 
 MUTANTS = {
     "unbiased-variance": ("layer_norm", _ln_unbiased),
@@ -103,6 +123,7 @@ MUTANTS = {
     "causal-excludes-self": ("attention", _attention_causal_strict),
     "gate-wrong-modality": ("gated_residual", _residual_wrong_index),
     "audio-step-major": ("packed_layout", _layout_audio_step_major),
+    "varlen-boundary-off-by-one": ("attention_varlen", _varlen_boundary_off_by_one),
 }
 
 PIN_TESTS = [getattr(pins, n) for n in dir(pins) if n.startswith("test_")]

@@ -360,3 +360,47 @@ def test_block_special_weights_reduce_to_parts():
         rcs = orc.block_rows(x, mod, pos, shift, scale, gate, wqkv, wo, rows, H,
                              causal=causal)
         np.testing.assert_allclose(rcs["out"], rc["out"][rows], atol=1e-12)
+
+
+# ------------------------------------------------------- varlen attention (NEXT f1)
+def test_varlen_visibility_matches_the_pages_example():
+    """Brute force over exactly the keys the pages' example makes visible."""
+    rng = np.random.default_rng(12)
+    H, dh = 1, 128
+    d = H * dh
+    for line in _read_table("cu_seqlens_example.txt"):
+        cu_s, q_s, lo_s, hi_s = line.split("|")
+        cu = [int(v) for v in cu_s.split()]
+        i, lo, hi = int(q_s), int(lo_s), int(hi_s)
+        L = cu[-1]
+        qkv = rng.normal(size=(L, 3 * d)) * 1.3
+        o, _ = orc.attention_varlen(qkv, cu, H, dh, rows=np.array([i]))
+        q = qkv[i, :d]
+        s = {j: math.fsum(q[c] * qkv[j, d + c] for c in range(dh)) / math.sqrt(dh)
+             for j in range(lo, hi + 1)}
+        m = max(s.values())
+        w = {j: math.exp(s[j] - m) for j in s}
+        z = math.fsum(w.values())
+        for c in range(0, dh, 9):
+            ref = math.fsum(w[j] * qkv[j, 2 * d + c] for j in s) / z
+            assert abs(o[0, c] - ref) < 1e-12
+        # keys and values outside the visible range carry zero weight
+        qkv2 = qkv.copy()
+        outside = [j for j in range(L) if not lo <= j <= hi]
+        qkv2[outside, d:] = rng.normal(size=(len(outside), 2 * d)) * 5
+        o2, _ = orc.attention_varlen(qkv2, cu, H, dh, rows=np.array([i]))
+        assert np.array_equal(o, o2)
+
+
+def test_varlen_reduces_to_full_and_causal_within_segments():
+    rng = np.random.default_rng(13)
+    L, H, dh = 41, 2, 128
+    qkv = rng.normal(size=(L, 3 * H * dh))
+    full, lse_f = orc.attention(qkv, H, dh)
+    one, lse_1 = orc.attention_varlen(qkv, [0, L], H, dh)
+    assert np.array_equal(full, one) and np.array_equal(lse_f, lse_1)
+    cu = [0, 7, 7, 30, 41]                     # an empty segment is allowed
+    oc, _ = orc.attention_varlen(qkv, cu, H, dh, causal=True)
+    for i, (lo, hi) in ((3, (0, 7)), (7, (7, 30)), (29, (7, 30)), (40, (30, 41))):
+        op, _ = orc.attention(qkv[lo:i + 1], H, dh, rows=np.array([i - lo]))
+        np.testing.assert_allclose(oc[i], op[0], atol=1e-12)
