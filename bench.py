@@ -346,6 +346,22 @@ def run_gpu(args, cfg):
     sweep_total = sev[0].elapsed_time(sev[50])
     del xs
 
+    # ---- block-diagonal attention over the modality segments (cu_seqlens
+    # [0, T, T+V, L]) on this step's rotated qkv, timed on its own
+    cu = [0, cfg.n_text, cfg.n_text + cfg.n_video, L]
+    qkv_ws = ws[(L * d * 2 + 255) // 256 * 256:][:L * 3 * d * 2].view(torch.bfloat16).view(L, 3 * d)
+    o_var = torch.empty(L, d, dtype=torch.bfloat16, device=dev)
+    h3.h3_joint_attn_varlen_fwd(qkv_ws, cu, L, H, 128, 0, None, o_var, stream=stream)
+    vev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    vev[0].record(stream)
+    for _ in range(5):
+        h3.h3_joint_attn_varlen_fwd(qkv_ws, cu, L, H, 128, 0, None, o_var, stream=stream)
+    vev[1].record(stream)
+    torch.cuda.synchronize(dev)
+    varlen_ms = vev[0].elapsed_time(vev[1]) / 5
+    varlen_flops = 4.0 * d * sum((cu[i + 1] - cu[i]) ** 2 for i in range(3))
+    del o_var
+
     flops = cfg.flops()
     value = world * flops / (ms * 1e-3) / 1e12
     attn_flops = 4.0 * L * L * d
@@ -388,6 +404,10 @@ def run_gpu(args, cfg):
                     "sustained_tflops": 50 * flops / (sweep_total * 1e-3) / 1e12,
                     "frac_of_sustained_bf16_peak":
                         50 * flops / (sweep_total * 1e-3) / 1e12 / peak},
+        "attn_varlen_modality": {"cu_seqlens": cu, "ms": varlen_ms,
+                                 "tflops": varlen_flops / (varlen_ms * 1e-3) / 1e12,
+                                 "frac_of_sustained_bf16_peak":
+                                     varlen_flops / (varlen_ms * 1e-3) / 1e12 / peak},
         "gpu_launches": 4 * args.steps,
         "clocks": clocks,
         "wall_s_timed": wall,

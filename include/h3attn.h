@@ -80,7 +80,12 @@ typedef struct {
   float ln_eps;         /* LayerNorm epsilon (>= 0), e.g. 1e-6 */
   int32_t causal;       /* 0: full bidirectional attention; 1: key index <= query index */
   int32_t n_mod;        /* number of modalities (rows of shift/scale/gate) */
+  int32_t n_seg;        /* 0: attention over the whole sequence; else number of segments */
+  const int32_t* cu_seqlens; /* host [n_seg + 1] when n_seg > 0 (see h3_joint_attn_varlen_fwd) */
 } h3_block_desc;
+
+/* Largest number of segments a cu_seqlens array may describe. */
+#define H3_MAX_SEGMENTS 64
 
 /* Text for a status code (static storage). */
 const char* h3_status_string(h3_status s);
@@ -148,6 +153,22 @@ h3_status h3_joint_attn_fwd(const uint16_t* qkv, int32_t L, int32_t n_heads, int
                             h3_stream_t stream);
 
 /*
+ * Joint attention restricted to sub-sequences ([vLLM] §3 Packed Sequences and
+ * Modality Identity Preservation: cu_seqlens is a 1-D array of segment offsets
+ * and a token takes softmax only over the keys of its own segment; worked
+ * example [0, 10, 30]: token 15 sees keys 10..29).
+ *   cu_seqlens: HOST array [n_seg + 1], cu_seqlens[0] = 0, non-decreasing,
+ *   cu_seqlens[n_seg] = L, 1 <= n_seg <= H3_MAX_SEGMENTS (empty segments
+ *   allowed).  causal: additionally key index <= query index.  Other arguments
+ *   and layouts as h3_joint_attn_fwd.  Key blocks outside a CTA's segments are
+ *   not visited.
+ */
+h3_status h3_joint_attn_varlen_fwd(const uint16_t* qkv, const int32_t* cu_seqlens,
+                                   int32_t n_seg, int32_t L, int32_t n_heads, int32_t head_dim,
+                                   int32_t causal, float sm_scale, uint16_t* O, float* lse,
+                                   h3_stream_t stream);
+
+/*
  * Output projection + per-modality gated residual ([H3-RL] to_out.0 and the
  * AdaLN gate):  out[n] = x_res[n] + gate[mod[n]] * (O[n] Wo^T); fp32 epilogue.
  *   O [L][d] bf16, Wo [d][d] bf16, x_res [L][d] bf16, mod [L] uint8,
@@ -165,8 +186,9 @@ h3_status h3_workspace_size(const h3_block_desc* desc, size_t* bytes);
 /*
  * The whole sub-block ([vLLM] §1: the step run 50 times over 58,758 tokens):
  * modulate -> QKV projection with the rotary embedding applied in its
- * epilogue -> joint attention -> output projection with gated residual, four
- * launches on `stream`.  workspace: >= h3_workspace_size() bytes of device
+ * epilogue -> joint attention (over the whole sequence, or per segment when
+ * desc->n_seg > 0) -> output projection with gated residual, four launches on
+ * `stream`.  workspace: >= h3_workspace_size() bytes of device
  * memory, 256-byte aligned, owned by the caller, not read before written.
  *   x [L][d] bf16, mod [L] uint8, pos [L][3] int32, shift/scale/gate
  *   [n_mod][d] fp32, Wqkv [3d][d] bf16, Wo [d][d] bf16 -> out [L][d] bf16.

@@ -18,7 +18,8 @@ import numpy as np
 __all__ = [
     "H3Error", "BlockDesc", "load", "lib_path", "h3_version", "h3_status_string",
     "h3_build_packed_layout", "h3_adaln_modulate", "h3_qkv_proj", "h3_mrope_apply",
-    "h3_joint_attn_fwd", "h3_out_proj_gated_residual", "h3_workspace_size",
+    "h3_joint_attn_fwd", "h3_joint_attn_varlen_fwd", "h3_out_proj_gated_residual",
+    "h3_workspace_size",
     "h3_attn_block_fwd", "h3_sync_status", "h3_set_wait_limit_ns",
     "h3_selftest_wait_timeout", "h3_attn_block_fwd_profiled", "h3_attn_block_fwd_noalloc",
     "NOALLOC_SCRATCH_BYTES", "EXPORTED_SYMBOLS",
@@ -33,7 +34,8 @@ STATUS_NAMES = {0: "H3_OK", 1: "H3_ERR_INVALID_ARG", 2: "H3_ERR_UNSUPPORTED", 3:
 
 EXPORTED_SYMBOLS = (
     "h3_status_string", "h3_version", "h3_build_packed_layout", "h3_adaln_modulate",
-    "h3_qkv_proj", "h3_mrope_apply", "h3_joint_attn_fwd", "h3_out_proj_gated_residual",
+    "h3_qkv_proj", "h3_mrope_apply", "h3_joint_attn_fwd", "h3_joint_attn_varlen_fwd",
+    "h3_out_proj_gated_residual",
     "h3_workspace_size", "h3_attn_block_fwd", "h3_sync_status", "h3_set_wait_limit_ns",
     "h3_selftest_wait_timeout", "h3_attn_block_fwd_profiled", "h3_attn_block_fwd_noalloc",
 )
@@ -52,14 +54,24 @@ class BlockDesc(ctypes.Structure):
     _fields_ = [("L", ctypes.c_int32), ("d", ctypes.c_int32), ("n_heads", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("rope_sec", ctypes.c_int32 * 3),
                 ("rope_base", ctypes.c_float), ("ln_eps", ctypes.c_float),
-                ("causal", ctypes.c_int32), ("n_mod", ctypes.c_int32)]
+                ("causal", ctypes.c_int32), ("n_mod", ctypes.c_int32),
+                ("n_seg", ctypes.c_int32), ("cu_seqlens", ctypes.POINTER(ctypes.c_int32))]
 
     @classmethod
     def make(cls, L, d, n_heads, head_dim=128, rope_sec=(32, 48, 48), rope_base=10000.0,
-             ln_eps=1e-6, causal=False, n_mod=3) -> "BlockDesc":
-        return cls(int(L), int(d), int(n_heads), int(head_dim),
+             ln_eps=1e-6, causal=False, n_mod=3, cu_seqlens=None) -> "BlockDesc":
+        cu = None if cu_seqlens is None else _int32_array(cu_seqlens)
+        desc = cls(int(L), int(d), int(n_heads), int(head_dim),
                    (ctypes.c_int32 * 3)(*[int(s) for s in rope_sec]), float(rope_base),
-                   float(ln_eps), int(bool(causal)), int(n_mod))
+                   float(ln_eps), int(bool(causal)), int(n_mod),
+                   0 if cu is None else len(cu) - 1, cu)
+        desc._cu_keepalive = cu          # the struct points into this host array
+        return desc
+
+
+def _int32_array(values):
+    vals = [int(v) for v in values]
+    return (ctypes.c_int32 * len(vals))(*vals)
 
 
 _lib: Optional[ctypes.CDLL] = None
@@ -77,6 +89,8 @@ def _sig(lib):
     lib.h3_qkv_proj.argtypes = [_P, _P, _I, _I, _P, _P]
     lib.h3_mrope_apply.argtypes = [_P, _P, _I, _I, _I, _P, ctypes.c_float, _P]
     lib.h3_joint_attn_fwd.argtypes = [_P, _I, _I, _I, _I, ctypes.c_float, _P, _P, _P]
+    lib.h3_joint_attn_varlen_fwd.argtypes = [_P, _P, _I, _I, _I, _I, _I, ctypes.c_float, _P, _P,
+                                             _P]
     lib.h3_out_proj_gated_residual.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _P, _P]
     lib.h3_workspace_size.argtypes = [ctypes.POINTER(BlockDesc), ctypes.POINTER(ctypes.c_size_t)]
     lib.h3_attn_block_fwd.argtypes = [ctypes.POINTER(BlockDesc)] + [_P] * 9 + [ctypes.c_size_t,
@@ -178,6 +192,17 @@ def h3_joint_attn_fwd(qkv, L, n_heads, head_dim, causal, sm_scale, O, lse=None,
     _check("h3_joint_attn_fwd", load().h3_joint_attn_fwd(
         _addr(qkv), L, n_heads, head_dim, int(bool(causal)), sm_scale, _addr(O), _addr(lse),
         _stream(stream)))
+
+
+def h3_joint_attn_varlen_fwd(qkv, cu_seqlens, L, n_heads, head_dim, causal, sm_scale, O,
+                             lse=None, stream=None) -> None:
+    """``cu_seqlens``: host sequence [0, c1, ..., L] of segment offsets."""
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(head_dim)
+    cu = _int32_array(cu_seqlens)
+    _check("h3_joint_attn_varlen_fwd", load().h3_joint_attn_varlen_fwd(
+        _addr(qkv), ctypes.addressof(cu), len(cu) - 1, L, n_heads, head_dim, int(bool(causal)),
+        sm_scale, _addr(O), _addr(lse), _stream(stream)))
 
 
 def h3_out_proj_gated_residual(O, Wo, x_res, mod, gate, L, d, n_mod, out, stream=None) -> None:

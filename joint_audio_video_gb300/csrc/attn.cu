@@ -49,7 +49,19 @@ struct AttnDev {
   int num_pairs;
   int* status;
   uint64_t wait_ns;
+  int n_seg;                      // 0: one segment [0, L)
+  int32_t cu[kMaxSegments + 1];   // segment starts, cu[n_seg] = L
 };
+
+// Segment of token i: the last s with cu[s] <= i (skips empty segments).
+__device__ __forceinline__ int segment_of(const AttnDev& p, int i) {
+  int lo = 0, hi = p.n_seg - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (p.cu[mid] <= i) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -144,8 +156,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int h = blockIdx.x / p.num_pairs;
   if (p.causal) pair = p.num_pairs - 1 - pair;   // longest rows first
   const int q0 = pair * 256;
-  const int kv_end = p.causal ? min(p.L, q0 + 256) : p.L;
-  const int nblk = (kv_end + 127) / 128;
+  const int r_last = min(q0 + 255, p.L - 1);
+  // keys this CTA visits: the union of its rows' segments, cut at the diagonal
+  int kv_lo = 0, kv_hi = p.L;
+  if (p.n_seg > 0) {
+    kv_lo = p.cu[segment_of(p, q0)];
+    kv_hi = p.cu[segment_of(p, r_last) + 1];
+  }
+  if (p.causal) kv_hi = min(kv_hi, r_last + 1);
+  const int nblk = (kv_hi - kv_lo + 127) / 128;
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
@@ -192,8 +211,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t dst = sRing + stage * kTile;
           const int x = kv == 0 ? xk : xv;
           mbar_arrive_expect_tx(fb, kTile);
-          tma_load_2d(dst, &tm, fb, x, j * 128);
-          tma_load_2d(dst + kBox, &tm, fb, x + 64, j * 128);
+          tma_load_2d(dst, &tm, fb, x, kv_lo + j * 128);
+          tma_load_2d(dst + kBox, &tm, fb, x + 64, kv_lo + j * 128);
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
       }
@@ -295,6 +314,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tS = tmem + g * 128 + lane_off;
     const uint32_t tO = tmem + 256 + g * 128 + lane_off;
     const uint32_t bs = smem_u32(&bar_s[g]), bp = smem_u32(&bar_p[g]);
+    // keys visible to this row: its segment, up to itself when causal
+    int row_lo = 0, row_hi = p.L;
+    if (p.n_seg > 0) {
+      const int sg = segment_of(p, min(qi, p.L - 1));
+      row_lo = p.cu[sg];
+      row_hi = p.cu[sg + 1];
+    }
+    if (p.causal) row_hi = min(row_hi, qi + 1);
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < nblk; ++j) {
@@ -310,27 +337,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld_wait(r1);
       tmem_ld_wait(r2);
       tmem_ld_wait(r3);
-      const int kv0 = j * 128;
-      const bool tail = kv0 + 128 > p.L;
-      const bool diag = p.causal && kv0 + 127 > tile_q0;
-      if (tail || diag) {
-        const int lim = (p.causal ? min(p.L - 1, qi) : p.L - 1) - kv0;   // last visible key
+      // block columns c are keys kv_lo + 128 j + c; visible iff lo_rel <= c < hi_rel
+      const int kv0 = kv_lo + j * 128;
+      const int lo_rel = row_lo - kv0, hi_rel = row_hi - kv0;
+      if (__any_sync(0xffffffffu, lo_rel > 0 || hi_rel < 128)) {
         constexpr uint32_t kNegInf = 0xFF800000u;
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
-          if (c > lim) r0[c] = kNegInf;
-          if (c + 32 > lim) r1[c] = kNegInf;
-          if (c + 64 > lim) r2[c] = kNegInf;
-          if (c + 96 > lim) r3[c] = kNegInf;
+          if (c < lo_rel || c >= hi_rel) r0[c] = kNegInf;
+          if (c + 32 < lo_rel || c + 32 >= hi_rel) r1[c] = kNegInf;
+          if (c + 64 < lo_rel || c + 64 >= hi_rel) r2[c] = kNegInf;
+          if (c + 96 < lo_rel || c + 96 >= hi_rel) r3[c] = kNegInf;
         }
       }
-      // row maximum of the raw scores (scale > 0 commutes with max)
+      // row maximum of the raw scores (scale > 0 commutes with max); -inf while
+      // no key of this row has been seen, and then O and l hold only zeros
       const float mx = fmaxf(max3(max32(r0), max32(r1), max32(r2)), max32(r3)) * p.scale_log2;
-      if (j == 0) {
-        m_used = mx;
-      } else {
+      {
         const float m_new = fmaxf(m_used, mx);
-        const bool need = m_new > m_used + kRescaleThreshold;
+        const bool fresh = m_used == -INFINITY;
+        const bool need = !fresh && m_new > m_used + kRescaleThreshold;
+        if (fresh) m_used = m_new;
         if (__any_sync(0xffffffffu, need)) {
           const float f = need ? ex2(m_used - m_new) : 1.f;
 #pragma unroll 1
@@ -348,7 +375,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       // p = 2^(s * scale_log2 - m_used), rounded to bf16 pairs over S's first 64 columns
-      const uint64_t cc = f2(p.scale_log2, p.scale_log2), nm = f2(-m_used, -m_used);
+      const float neg_m = m_used == -INFINITY ? 0.f : -m_used;   // all scores -inf: p = 0
+      const uint64_t cc = f2(p.scale_log2, p.scale_log2), nm = f2(neg_m, neg_m);
       uint64_t acc[2] = {0ull, 0ull};
       uint32_t pk0[32], pk1[32];
       exp32(r0, cc, nm, pk0, acc);
@@ -415,6 +443,8 @@ cudaError_t launch_attention(const AttnArgs& a, const DevCtx& ctx, cudaStream_t 
   p.num_pairs = (a.L + 255) / 256;
   p.status = ctx.status;
   p.wait_ns = ctx.wait_ns;
+  p.n_seg = a.n_seg;
+  for (int i = 0; i <= a.n_seg && a.cu_seqlens; ++i) p.cu[i] = a.cu_seqlens[i];
   cudaError_t e =
       cudaFuncSetAttribute(attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmem));
   if (e != cudaSuccess) return e;

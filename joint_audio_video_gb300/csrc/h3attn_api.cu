@@ -78,6 +78,15 @@ h3_status check_rope(const int32_t sec[3], int32_t head_dim, float base) {
 
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// cu_seqlens: host array, 0 = c_0 <= c_1 <= ... <= c_n = L, 1 <= n <= kMaxSegments.
+h3_status check_segments(const int32_t* cu, int32_t n_seg, int32_t L) {
+  if (n_seg < 1 || n_seg > kMaxSegments || cu == nullptr) return H3_ERR_INVALID_ARG;
+  if (cu[0] != 0 || cu[n_seg] != L) return H3_ERR_INVALID_ARG;
+  for (int s = 0; s < n_seg; ++s)
+    if (cu[s + 1] < cu[s]) return H3_ERR_INVALID_ARG;
+  return H3_OK;
+}
+
 // ------------------------------------------------------------------ self-test kernel
 __global__ void wait_selftest_kernel(int* status, uint64_t limit_ns) {
   __shared__ uint64_t bar;
@@ -198,6 +207,35 @@ h3_status h3_joint_attn_fwd(const uint16_t* qkv, int32_t L, int32_t n_heads, int
   return launched(launch_attention(a, ctx, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+h3_status h3_joint_attn_varlen_fwd(const uint16_t* qkv, const int32_t* cu_seqlens,
+                                   int32_t n_seg, int32_t L, int32_t n_heads, int32_t head_dim,
+                                   int32_t causal, float sm_scale, uint16_t* O, float* lse,
+                                   h3_stream_t stream) {
+  if (L < 1 || n_heads < 1) return H3_ERR_INVALID_ARG;
+  if (head_dim != 128) return H3_ERR_UNSUPPORTED;
+  if (!valid_d(n_heads * 128)) return H3_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return H3_ERR_INVALID_ARG;
+  if (!(sm_scale > 0.f) || !std::isfinite(sm_scale)) return H3_ERR_INVALID_ARG;
+  if (h3_status s = check_segments(cu_seqlens, n_seg, L)) return s;
+  if (!aligned16(qkv) || !aligned16(O)) return H3_ERR_INVALID_ARG;
+  if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u)) return H3_ERR_INVALID_ARG;
+  const size_t d = size_t(n_heads) * 128;
+  if (overlap(qkv, size_t(L) * 3 * d * 2, O, size_t(L) * d * 2)) return H3_ERR_INVALID_ARG;
+  DevCtx ctx;
+  if (h3_status s = dev_ctx(&ctx)) return s;
+  AttnArgs a{};
+  a.qkv = qkv;
+  a.O = O;
+  a.lse = lse;
+  a.L = L;
+  a.H = n_heads;
+  a.causal = causal;
+  a.sm_scale = sm_scale;
+  a.n_seg = n_seg;
+  a.cu_seqlens = cu_seqlens;
+  return launched(launch_attention(a, ctx, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 h3_status h3_out_proj_gated_residual(const uint16_t* O, const uint16_t* Wo,
                                      const uint16_t* x_res, const uint8_t* mod,
                                      const float* gate, int32_t L, int32_t d, int32_t n_mod,
@@ -234,6 +272,9 @@ static h3_status check_desc(const h3_block_desc* desc) {
   if (desc->d != desc->n_heads * desc->head_dim || !valid_d(desc->d)) return H3_ERR_INVALID_ARG;
   if (desc->causal != 0 && desc->causal != 1) return H3_ERR_INVALID_ARG;
   if (!(desc->ln_eps >= 0.f) || !std::isfinite(desc->ln_eps)) return H3_ERR_INVALID_ARG;
+  if (desc->n_seg != 0) {
+    if (h3_status s = check_segments(desc->cu_seqlens, desc->n_seg, desc->L)) return s;
+  }
   return check_rope(desc->rope_sec, desc->head_dim, desc->rope_base);
 }
 
@@ -312,6 +353,8 @@ h3_status h3_attn_block_fwd_profiled(const h3_block_desc* desc, const uint16_t* 
   a.H = desc->n_heads;
   a.causal = desc->causal;
   a.sm_scale = 1.0f / std::sqrt(float(desc->head_dim));
+  a.n_seg = desc->n_seg;
+  a.cu_seqlens = desc->cu_seqlens;
   if (launch_attention(a, ctx, st) != cudaSuccess || !mark(3)) return H3_ERR_CUDA;
 
   GemmArgs o{};

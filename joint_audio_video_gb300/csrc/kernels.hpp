@@ -51,6 +51,8 @@ struct GemmArgs {
 
 cudaError_t launch_gemm(const GemmArgs& a, const DevCtx& ctx, cudaStream_t st);
 
+constexpr int kMaxSegments = 64;
+
 struct AttnArgs {
   const void* qkv;      // [L][3*H*128] bf16
   void* O;              // [L][H*128] bf16
@@ -58,6 +60,8 @@ struct AttnArgs {
   int L, H;
   int causal;
   float sm_scale;
+  int n_seg;                  // 0: one segment [0, L)
+  const int32_t* cu_seqlens;  // host array [n_seg + 1], validated, n_seg <= kMaxSegments
 };
 
 cudaError_t launch_attention(const AttnArgs& a, const DevCtx& ctx, cudaStream_t st);

@@ -233,12 +233,16 @@ def block(x: np.ndarray, mod: np.ndarray, pos: np.ndarray, shift: np.ndarray,
           scale: np.ndarray, gate: np.ndarray, wqkv: np.ndarray, wo: np.ndarray,
           n_heads: int, head_dim: int = 128, causal: bool = False,
           eps: float = 1e-6, sections: Sequence[int] = (32, 48, 48),
-          base: float = 10000.0) -> Dict[str, np.ndarray]:
-    """Every intermediate of the block forward for all L tokens."""
+          base: float = 10000.0, cu_seqlens=None) -> Dict[str, np.ndarray]:
+    """Every intermediate of the block forward for all L tokens (attention
+    restricted to the segments of ``cu_seqlens`` when given)."""
     y = adaln_modulate(x, mod, shift, scale, eps)
     qkv_pre = linear(y, wqkv)
     qkv = mrope(qkv_pre, pos, n_heads, head_dim, sections, base)
-    o, lse = attention(qkv, n_heads, head_dim, causal)
+    if cu_seqlens is None:
+        o, lse = attention(qkv, n_heads, head_dim, causal)
+    else:
+        o, lse = attention_varlen(qkv, cu_seqlens, n_heads, head_dim, causal)
     branch = linear(o, wo)
     out = gated_residual(x, branch, mod, gate)
     return {"y": y, "qkv_pre": qkv_pre, "qkv": qkv, "O": o, "lse": lse,

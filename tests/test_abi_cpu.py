@@ -30,7 +30,7 @@ def _declared():
 
 def test_library_exports_every_declared_entry_point(lib):
     names = _declared()
-    assert len(names) == 15, names
+    assert len(names) == 16, names
     raw = ctypes.CDLL(lib.lib_path)
     for n in names:
         assert hasattr(raw, n), f"{n} declared but not exported"
@@ -133,3 +133,27 @@ def test_host_layout_rejects_bad_counts(lib):
     mod = np.zeros(4, np.uint8)
     pos = np.zeros((4, 3), np.int32)
     assert L.h3_build_packed_layout(3, 1, 1, 2, 0, 0, mod.ctypes.data, pos.ctypes.data, 4) == 1
+
+
+def test_segment_arrays_are_validated_before_launch(lib):
+    L = lib.load()
+    p = 1 << 20
+    out = p + (1 << 24)
+    import ctypes as C
+
+    def call(cu, n_seg=None, Lt=45):
+        arr = (C.c_int32 * len(cu))(*cu) if cu is not None else None
+        n = len(cu) - 1 if n_seg is None else n_seg
+        return L.h3_joint_attn_varlen_fwd(p, C.addressof(arr) if arr is not None else None, n, Lt,
+                                          1, 128, 0, 0.088, out, None, None)
+    assert call([1, 10, 45]) == 1            # does not start at 0
+    assert call([0, 30, 10, 45]) == 1        # decreasing
+    assert call([0, 10, 44]) == 1            # does not end at L
+    assert call([0, 45], n_seg=0) == 1       # no segment
+    assert call(None, n_seg=1) == 1          # NULL array
+    assert call(list(range(0, 66)) + [45], Lt=45) == 1   # more than 64 segments
+    with pytest.raises(lib.H3Error) as e:
+        lib.h3_workspace_size(lib.BlockDesc.make(L=45, d=256, n_heads=2, cu_seqlens=[0, 10, 44]))
+    assert e.value.status == 1
+    assert lib.h3_workspace_size(lib.BlockDesc.make(L=45, d=256, n_heads=2,
+                                                    cu_seqlens=[0, 10, 30, 45])) > 0
