@@ -92,13 +92,39 @@ __device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
-// Maximum of 32 raw scores as a chain of 16 three-input max operations.
-__device__ __forceinline__ float max32(const uint32_t (&r)[32]) {
-  float m = max3(__uint_as_float(r[0]), __uint_as_float(r[1]), __uint_as_float(r[2]));
+#define H3_F(x) __uint_as_float(x)
+// Maximum of the 128 raw scores of a row as 8 interleaved chains of 8
+// three-input max operations (short dependency chains), then a 3-level tree.
+__device__ __forceinline__ float max128(const uint32_t (&r0)[32], const uint32_t (&r1)[32],
+                                       const uint32_t (&r2)[32], const uint32_t (&r3)[32]) {
+  float m[8];
 #pragma unroll
-  for (int i = 3; i < 31; i += 2) m = max3(m, __uint_as_float(r[i]), __uint_as_float(r[i + 1]));
-  return fmaxf(m, __uint_as_float(r[31]));
+  for (int q = 0; q < 2; ++q) {
+    m[0 + q] = max3(H3_F(r0[16 * q]), H3_F(r0[16 * q + 1]), H3_F(r0[16 * q + 2]));
+    m[2 + q] = max3(H3_F(r1[16 * q]), H3_F(r1[16 * q + 1]), H3_F(r1[16 * q + 2]));
+    m[4 + q] = max3(H3_F(r2[16 * q]), H3_F(r2[16 * q + 1]), H3_F(r2[16 * q + 2]));
+    m[6 + q] = max3(H3_F(r3[16 * q]), H3_F(r3[16 * q + 1]), H3_F(r3[16 * q + 2]));
+  }
+#pragma unroll
+  for (int i = 3; i < 15; i += 2) {
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      m[0 + q] = max3(m[0 + q], H3_F(r0[16 * q + i]), H3_F(r0[16 * q + i + 1]));
+      m[2 + q] = max3(m[2 + q], H3_F(r1[16 * q + i]), H3_F(r1[16 * q + i + 1]));
+      m[4 + q] = max3(m[4 + q], H3_F(r2[16 * q + i]), H3_F(r2[16 * q + i + 1]));
+      m[6 + q] = max3(m[6 + q], H3_F(r3[16 * q + i]), H3_F(r3[16 * q + i + 1]));
+    }
+  }
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    m[0 + q] = fmaxf(m[0 + q], H3_F(r0[16 * q + 15]));
+    m[2 + q] = fmaxf(m[2 + q], H3_F(r1[16 * q + 15]));
+    m[4 + q] = fmaxf(m[4 + q], H3_F(r2[16 * q + 15]));
+    m[6 + q] = fmaxf(m[6 + q], H3_F(r3[16 * q + 15]));
+  }
+  return fmaxf(max3(m[0], m[1], m[2]), max3(m[3], m[4], max3(m[5], m[6], m[7])));
 }
+#undef H3_F
 // p = 2^(s*c - m) for 32 raw scores: 16 bf16 pairs into pk, row sum into acc.
 __device__ __forceinline__ void exp32(const uint32_t (&r)[32], uint64_t cc, uint64_t nm,
                                       uint32_t* pk, uint64_t (&acc)[2]) {
@@ -352,7 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // row maximum of the raw scores (scale > 0 commutes with max); -inf while
       // no key of this row has been seen, and then O and l hold only zeros
-      const float mx = fmaxf(max3(max32(r0), max32(r1), max32(r2)), max32(r3)) * p.scale_log2;
+      const float mx = max128(r0, r1, r2, r3) * p.scale_log2;
       {
         const float m_new = fmaxf(m_used, mx);
         const bool fresh = m_used == -INFINITY;
