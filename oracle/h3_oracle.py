@@ -283,3 +283,42 @@ def block_rows(x: np.ndarray, mod: np.ndarray, pos: np.ndarray,
     out = gated_residual(x[rows], branch, mod[rows], gate)
     return {"y": y[rows], "q": q_rot, "k": k_rot, "v": kv_pre[:, d:],
             "O": o, "lse": lse, "branch": branch, "out": out}
+
+
+# ---------------------------------------------------------------------------
+# NEXT f2: one denoising-step update of the packed latent ([vLLM] §4
+#   Denoising Execution Flow, stages 5-7; [VeRL] 5.1 timestep convention)
+# ---------------------------------------------------------------------------
+def sigma_to_t_h3(sigma):
+    """H3's data-progress time for a noise level: t_H3 = 1 - sigma ([VeRL] 5.1)."""
+    return 1.0 - np.asarray(sigma, dtype=np.float64)
+
+
+def denoise_step(z: np.ndarray, v_h3: np.ndarray, mod: np.ndarray, sigma, sigma_next,
+                 update, anchor: Optional[np.ndarray] = None,
+                 z_anchor: Optional[np.ndarray] = None) -> Tuple[np.ndarray, np.ndarray]:
+    """One deterministic (eta = 0) Euler step of the packed latent.
+
+    ``z [L, C]`` is the state at noise level ``sigma[mod[n]]`` (one schedule per
+    modality), ``v_h3 [L, C]`` the DiT's velocity in H3's sign (data-progress
+    time), ``update[m]`` says whether modality m is a denoised latent (text
+    rows are conditions and stay as they are).  With the straight path
+    z = (1 - sigma) x0 + sigma eps the standard velocity is v = eps - x0 =
+    -v_h3, the clean estimate is x0 = z - sigma v (rectified-flow v -> X0) and
+    the Euler step to ``sigma_next`` is z + (sigma_next - sigma) v.  Rows with
+    ``anchor[n]`` set are re-pinned to ``z_anchor[n]`` afterwards.
+    Returns (z_next, x0_hat); rows that are not updated keep z in both.
+    """
+    m = mod.astype(np.int64)
+    sig = np.asarray(sigma, dtype=np.float64)[m][:, None]
+    sig_n = np.asarray(sigma_next, dtype=np.float64)[m][:, None]
+    upd = np.asarray(update, dtype=bool)[m][:, None]
+    v = -v_h3
+    x0 = np.where(upd, z - sig * v, z)
+    z_next = np.where(upd, z + (sig_n - sig) * v, z)
+    if anchor is not None:
+        a = np.asarray(anchor, dtype=bool)[:, None]
+        z_next = np.where(a, z_anchor, z_next)
+        x0 = np.where(a, z_anchor, x0)
+    return z_next, x0
+

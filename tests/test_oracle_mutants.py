@@ -93,6 +93,18 @@ def _varlen_boundary_off_by_one(qkv, cu_seqlens, n_heads, head_dim=128, causal=F
     return out, lse
 
 
+def _denoise_native_sign(z, v_h3, mod, sigma, sigma_next, update, anchor=None, z_anchor=None):
+    """Uses H3's velocity without the sign reversal."""
+    return _ORIG["denoise_step"](z, -v_h3, mod, sigma, sigma_next, update, anchor, z_anchor)
+
+
+def _denoise_shared_schedule(z, v_h3, mod, sigma, sigma_next, update, anchor=None,
+                             z_anchor=None):
+    """Applies the video schedule to every modality."""
+    s = np.full(len(sigma), sigma[1]); sn = np.full(len(sigma_next), sigma_next[1])
+    return _ORIG["denoise_step"](z, v_h3, mod, s, sn, update, anchor, z_anchor)
+
+
 def _residual_wrong_index(x, branch, mod, gate):
     return x + gate[(mod.astype(np.int64) + 1) % 3] * branch
 
@@ -110,7 +122,8 @@ def _layout_audio_step_major(n_text, vt, vh, vw, ac, steps):
 
 _ORIG = {name: getattr(core, name) for name in
          ("layer_norm", "adaln_modulate", "linear", "rope_rotate_heads",
-          "rope_angles", "attention", "attention_varlen", "gated_residual", "packed_layout")}
+          "rope_angles", "attention", "attention_varlen", "gated_residual", "packed_layout",
+          "denoise_step")}
 
 MUTANTS = {
     "unbiased-variance": ("layer_norm", _ln_unbiased),
@@ -124,6 +137,8 @@ MUTANTS = {
     "gate-wrong-modality": ("gated_residual", _residual_wrong_index),
     "audio-step-major": ("packed_layout", _layout_audio_step_major),
     "varlen-boundary-off-by-one": ("attention_varlen", _varlen_boundary_off_by_one),
+    "denoise-native-velocity-sign": ("denoise_step", _denoise_native_sign),
+    "denoise-shared-schedule": ("denoise_step", _denoise_shared_schedule),
 }
 
 PIN_TESTS = [getattr(pins, n) for n in dir(pins) if n.startswith("test_")]

@@ -404,3 +404,57 @@ def test_varlen_reduces_to_full_and_causal_within_segments():
     for i, (lo, hi) in ((3, (0, 7)), (7, (7, 30)), (29, (7, 30)), (40, (30, 41))):
         op, _ = orc.attention(qkv[lo:i + 1], H, dh, rows=np.array([i - lo]))
         np.testing.assert_allclose(oc[i], op[0], atol=1e-12)
+
+
+# ------------------------------------------------------- denoise step (NEXT f2)
+def _straight_path(rng, L, C):
+    x0 = rng.normal(size=(L, C))
+    eps = rng.normal(size=(L, C))
+    return x0, eps
+
+
+def test_denoise_step_recovers_a_straight_path_exactly():
+    """With the exact velocity of z = (1-s) x0 + s eps (H3 sign: x0 - eps), the
+    clean estimate is x0 at any noise level and one Euler step lands on the
+    path at the next level."""
+    rng = np.random.default_rng(20)
+    L, C = 12, 16
+    mod = np.array([0, 1, 1, 2, 2, 1, 0, 2, 1, 1, 2, 2], dtype=np.uint8)
+    x0, eps = _straight_path(rng, L, C)
+    sig, sig_n = np.array([0.0, 0.8, 0.6]), np.array([0.0, 0.55, 0.2])
+    s = sig[mod.astype(int)][:, None]
+    sn = sig_n[mod.astype(int)][:, None]
+    z = (1 - s) * x0 + s * eps
+    z_next, x0_hat = orc.denoise_step(z, x0 - eps, mod, sig, sig_n, [0, 1, 1])
+    lat = mod > 0
+    np.testing.assert_allclose(x0_hat[lat], x0[lat], atol=1e-12)
+    np.testing.assert_allclose(z_next[lat], ((1 - sn) * x0 + sn * eps)[lat], atol=1e-12)
+    assert np.array_equal(z_next[~lat], z[~lat]) and np.array_equal(x0_hat[~lat], z[~lat])
+    assert np.allclose(orc.sigma_to_t_h3([1.0, 0.25, 0.0]), [0.0, 0.75, 1.0])
+
+
+def test_denoise_three_step_trace_reaches_clean_latents():
+    sched = {}
+    for line in _read_table("denoise_trace.txt"):
+        name, vals = line.split("|")
+        sched[name.strip()] = [float(v) for v in vals.split()]
+    rng = np.random.default_rng(21)
+    L, C = 10, 8
+    mod = np.array([0, 1, 1, 1, 1, 2, 2, 2, 1, 2], dtype=np.uint8)
+    anchor = np.zeros(L, dtype=np.uint8)
+    anchor[[2, 6]] = 1
+    x0, eps = _straight_path(rng, L, C)
+    z_anchor = rng.normal(size=(L, C))
+    z = eps.copy()                                     # pure noise at sigma_max = 1
+    z[anchor.astype(bool)] = z_anchor[anchor.astype(bool)]
+    for k in range(3):
+        sig = [0.0, sched["video"][k], sched["audio"][k]]
+        sig_n = [0.0, sched["video"][k + 1], sched["audio"][k + 1]]
+        s = np.asarray(sig)[mod.astype(int)][:, None]
+        v_h3 = x0 - eps                                # exact velocity, H3 sign
+        z, x0_hat = orc.denoise_step(z, v_h3, mod, sig, sig_n, [0, 1, 1], anchor, z_anchor)
+        a = anchor.astype(bool)
+        assert np.array_equal(z[a], z_anchor[a])      # re-pinned every step
+    free = (mod > 0) & ~anchor.astype(bool)
+    np.testing.assert_allclose(z[free], x0[free], atol=1e-12)
+    assert np.array_equal(z[mod == 0], eps[mod == 0])  # text rows never move
