@@ -362,6 +362,29 @@ def run_gpu(args, cfg):
     varlen_flops = 4.0 * d * sum((cu[i + 1] - cu[i]) ** 2 for i in range(3))
     del o_var
 
+    # ---- one denoising-step update of the packed latent (C = 96 channels per
+    # token: 24 latent channels x 1x2x2 patch), HBM-bound; L2 flushed between runs
+    C_lat = 96
+    zl = torch.randn(L, C_lat, device=dev)
+    vl = torch.randn(L, C_lat, device=dev).to(torch.bfloat16)
+    x0l = torch.empty_like(zl)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    dts = []
+    for it in range(6):
+        flush.fill_(it)
+        e_a, e_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e_a.record(stream)
+        h3.h3_denoise_step(zl, x0l, vl, mod_d, None, None, L, C_lat, [0.0, 0.6, 0.4],
+                           [0.0, 0.5, 0.3], [0, 1, 1], stream=stream)
+        e_b.record(stream)
+        torch.cuda.synchronize(dev)
+        if it > 0:
+            dts.append(e_a.elapsed_time(e_b))
+    denoise_ms = statistics.median(dts)
+    lat_rows = L - cfg.n_text
+    denoise_bytes = lat_rows * C_lat * (4 + 2 + 4 + 4) + cfg.n_text * C_lat * 8
+    del zl, vl, x0l, flush
+
     flops = cfg.flops()
     value = world * flops / (ms * 1e-3) / 1e12
     attn_flops = 4.0 * L * L * d
@@ -408,6 +431,10 @@ def run_gpu(args, cfg):
                                  "tflops": varlen_flops / (varlen_ms * 1e-3) / 1e12,
                                  "frac_of_sustained_bf16_peak":
                                      varlen_flops / (varlen_ms * 1e-3) / 1e12 / peak},
+        "denoise_step": {"L": L, "C": C_lat, "ms": denoise_ms,
+                         "gbs": denoise_bytes / (denoise_ms * 1e-3) / 1e9,
+                         "frac_of_hbm_peak": denoise_bytes / (denoise_ms * 1e-3) / 1e9
+                         / float(peaks["hbm_gbs"])},
         "gpu_launches": 4 * args.steps,
         "clocks": clocks,
         "wall_s_timed": wall,

@@ -180,6 +180,27 @@ h3_status h3_out_proj_gated_residual(const uint16_t* O, const uint16_t* Wo,
                                      const float* gate, int32_t L, int32_t d, int32_t n_mod,
                                      uint16_t* out, h3_stream_t stream);
 
+/*
+ * One denoising-step update of the packed latent ([vLLM] §4 Denoising
+ * Execution Flow, stages 5-7; [VeRL] 5.1: H3 time t = 1 - sigma, H3 velocity
+ * = minus the standard flow-matching velocity).  For each token n with
+ * modality m = mod[n] and update[m] != 0, with v = -v_h3[n]:
+ *   x0[n] = z[n] - sigma[m] v            (rectified-flow clean estimate)
+ *   z[n]  = z[n] + (sigma_next[m] - sigma[m]) v   (deterministic Euler step)
+ * Rows with update[m] == 0 (conditions such as text) keep z (x0 = z).  Rows
+ * with anchor[n] != 0 are re-pinned: z[n] = x0[n] = z_anchor[n].
+ *   z [L][C] fp32 device, in place; x0 [L][C] fp32 device or NULL;
+ *   v_h3 [L][C] bf16 device; mod [L] uint8 device; anchor [L] uint8 device or
+ *   NULL (then z_anchor is ignored), z_anchor [L][C] fp32 device.
+ *   sigma, sigma_next [n_mod] fp32 and update [n_mod] uint8: HOST arrays,
+ *   0 <= sigma <= 1.  C % 4 == 0.  A modality id >= n_mod leaves its row
+ *   unchanged and flags H3_ERR_BAD_INDEX.
+ */
+h3_status h3_denoise_step(float* z, float* x0, const uint16_t* v_h3, const uint8_t* mod,
+                          const uint8_t* anchor, const float* z_anchor, int32_t L, int32_t C,
+                          int32_t n_mod, const float* sigma, const float* sigma_next,
+                          const uint8_t* update, h3_stream_t stream);
+
 /* Bytes of device workspace h3_attn_block_fwd needs for `desc`. */
 h3_status h3_workspace_size(const h3_block_desc* desc, size_t* bytes);
 

@@ -22,7 +22,7 @@ __all__ = [
     "h3_workspace_size",
     "h3_attn_block_fwd", "h3_sync_status", "h3_set_wait_limit_ns",
     "h3_selftest_wait_timeout", "h3_attn_block_fwd_profiled", "h3_attn_block_fwd_noalloc",
-    "NOALLOC_SCRATCH_BYTES", "EXPORTED_SYMBOLS",
+    "h3_denoise_step", "NOALLOC_SCRATCH_BYTES", "EXPORTED_SYMBOLS",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -38,6 +38,7 @@ EXPORTED_SYMBOLS = (
     "h3_out_proj_gated_residual",
     "h3_workspace_size", "h3_attn_block_fwd", "h3_sync_status", "h3_set_wait_limit_ns",
     "h3_selftest_wait_timeout", "h3_attn_block_fwd_profiled", "h3_attn_block_fwd_noalloc",
+    "h3_denoise_step",
 )
 
 # Workspace the library keeps per GPU for h3_attn_block_fwd_noalloc.
@@ -98,6 +99,7 @@ def _sig(lib):
     lib.h3_attn_block_fwd_profiled.argtypes = (
         [ctypes.POINTER(BlockDesc)] + [_P] * 9 + [ctypes.c_size_t, _P, _P, _P])
     lib.h3_attn_block_fwd_noalloc.argtypes = [ctypes.POINTER(BlockDesc)] + [_P] * 10
+    lib.h3_denoise_step.argtypes = [_P] * 6 + [_I, _I, _I, _P, _P, _P, _P]
     lib.h3_sync_status.argtypes = [_P]
     lib.h3_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
     lib.h3_set_wait_limit_ns.restype = None
@@ -251,6 +253,19 @@ def h3_attn_block_fwd_noalloc(desc: BlockDesc, x, mod, pos, shift, scale, gate, 
     _check("h3_attn_block_fwd_noalloc", load().h3_attn_block_fwd_noalloc(
         ctypes.byref(desc), _addr(x), _addr(mod), _addr(pos), _addr(shift), _addr(scale),
         _addr(gate), _addr(Wqkv), _addr(Wo), _addr(out), _stream(stream)))
+
+
+def h3_denoise_step(z, x0, v_h3, mod, anchor, z_anchor, L, C, sigma, sigma_next, update,
+                    stream=None) -> None:
+    """``sigma``, ``sigma_next``, ``update``: host sequences, one entry per modality."""
+    n_mod = len(sigma)
+    sg = (ctypes.c_float * n_mod)(*[float(v) for v in sigma])
+    sn = (ctypes.c_float * n_mod)(*[float(v) for v in sigma_next])
+    up = (ctypes.c_uint8 * n_mod)(*[1 if u else 0 for u in update])
+    _check("h3_denoise_step", load().h3_denoise_step(
+        _addr(z), _addr(x0), _addr(v_h3), _addr(mod), _addr(anchor), _addr(z_anchor), L, C,
+        n_mod, ctypes.addressof(sg), ctypes.addressof(sn), ctypes.addressof(up),
+        _stream(stream)))
 
 
 def h3_sync_status(stream=None) -> int:

@@ -264,6 +264,31 @@ h3_status h3_out_proj_gated_residual(const uint16_t* O, const uint16_t* Wo,
   return launched(launch_gemm(a, ctx, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+h3_status h3_denoise_step(float* z, float* x0, const uint16_t* v_h3, const uint8_t* mod,
+                          const uint8_t* anchor, const float* z_anchor, int32_t L, int32_t C,
+                          int32_t n_mod, const float* sigma, const float* sigma_next,
+                          const uint8_t* update, h3_stream_t stream) {
+  if (L < 1 || C < 4 || C % 4 != 0 || n_mod < 1 || n_mod > 255) return H3_ERR_INVALID_ARG;
+  if (!aligned16(z) || !aligned16(v_h3) || mod == nullptr) return H3_ERR_INVALID_ARG;
+  if (x0 != nullptr && !aligned16(x0)) return H3_ERR_INVALID_ARG;
+  if (anchor != nullptr && !aligned16(z_anchor)) return H3_ERR_INVALID_ARG;
+  if (sigma == nullptr || sigma_next == nullptr || update == nullptr) return H3_ERR_INVALID_ARG;
+  const size_t n = size_t(L) * C;
+  if (x0 != nullptr && overlap(z, n * 4, x0, n * 4)) return H3_ERR_INVALID_ARG;
+  DenoiseParams dp{};
+  for (int m = 0; m < n_mod; ++m) {
+    if (!(sigma[m] >= 0.f && sigma[m] <= 1.f) || !(sigma_next[m] >= 0.f && sigma_next[m] <= 1.f))
+      return H3_ERR_INVALID_ARG;
+    dp.sigma[m] = sigma[m];
+    dp.sigma_next[m] = sigma_next[m];
+    dp.update[m] = update[m] ? 1 : 0;
+  }
+  DevCtx ctx;
+  if (h3_status s = dev_ctx(&ctx)) return s;
+  return launched(launch_denoise(z, x0, v_h3, mod, anchor, z_anchor, L, C, n_mod, dp, ctx,
+                                 reinterpret_cast<cudaStream_t>(stream)));
+}
+
 static h3_status check_desc(const h3_block_desc* desc) {
   if (desc == nullptr) return H3_ERR_INVALID_ARG;
   if (desc->L < 1 || desc->n_heads < 1 || desc->n_mod < 1 || desc->n_mod > 255)

@@ -66,6 +66,17 @@ struct AttnArgs {
 
 cudaError_t launch_attention(const AttnArgs& a, const DevCtx& ctx, cudaStream_t st);
 
+// Per-modality noise levels of one denoising step (host-validated).
+struct DenoiseParams {
+  float sigma[256];
+  float sigma_next[256];
+  uint8_t update[256];   // 1: the modality is a denoised latent; 0: a condition
+};
+
+cudaError_t launch_denoise(float* z, float* x0, const void* v_h3, const uint8_t* mod,
+                           const uint8_t* anchor, const float* z_anchor, int L, int C, int n_mod,
+                           const DenoiseParams& dp, const DevCtx& ctx, cudaStream_t st);
+
 cudaError_t launch_wait_selftest(const DevCtx& ctx, cudaStream_t st);
 
 }  // namespace h3

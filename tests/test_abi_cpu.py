@@ -30,7 +30,7 @@ def _declared():
 
 def test_library_exports_every_declared_entry_point(lib):
     names = _declared()
-    assert len(names) == 16, names
+    assert len(names) == 17, names
     raw = ctypes.CDLL(lib.lib_path)
     for n in names:
         assert hasattr(raw, n), f"{n} declared but not exported"
@@ -157,3 +157,23 @@ def test_segment_arrays_are_validated_before_launch(lib):
     assert e.value.status == 1
     assert lib.h3_workspace_size(lib.BlockDesc.make(L=45, d=256, n_heads=2,
                                                     cu_seqlens=[0, 10, 30, 45])) > 0
+
+
+def test_denoise_arguments_are_validated_before_launch(lib):
+    import ctypes as C
+    L = lib.load()
+    p = 1 << 20
+    s3 = (C.c_float * 3)(0.0, 0.5, 0.5)
+    bad = (C.c_float * 3)(0.0, 1.5, 0.5)
+    up = (C.c_uint8 * 3)(0, 1, 1)
+    a = lambda x: C.addressof(x)
+    assert L.h3_denoise_step(p, None, p + (1 << 24), p, None, None, 10, 6, 3, a(s3), a(s3), a(up),
+                             None) == 1                      # C not a multiple of 4
+    assert L.h3_denoise_step(p, None, p + (1 << 24), p, None, None, 10, 8, 3, a(bad), a(s3), a(up),
+                             None) == 1                      # sigma outside [0, 1]
+    assert L.h3_denoise_step(p, None, p + (1 << 24), p, None, None, 10, 8, 3, None, a(s3), a(up),
+                             None) == 1                      # missing host schedule
+    assert L.h3_denoise_step(p + 4, None, p + (1 << 24), p, None, None, 10, 8, 3, a(s3), a(s3),
+                             a(up), None) == 1               # misaligned state
+    assert L.h3_denoise_step(p, p + 16, p + (1 << 24), p, None, None, 10, 8, 3, a(s3), a(s3),
+                             a(up), None) == 1               # x0 overlapping z
