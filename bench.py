@@ -362,6 +362,29 @@ def run_gpu(args, cfg):
     varlen_flops = 4.0 * d * sum((cu[i + 1] - cu[i]) ** 2 for i in range(3))
     del o_var
 
+    # ---- the MLP sub-block of the same layer (hidden 4d), timed on its own
+    hid = 4 * d
+    gmlp = torch.Generator(device="cpu").manual_seed(11)
+    w1m = (torch.randn(hid, d, generator=gmlp) / d ** 0.5).to(torch.bfloat16).to(dev)
+    w2m = (torch.randn(d, hid, generator=gmlp) / hid ** 0.5).to(torch.bfloat16).to(dev)
+    mdesc = h3.MlpDesc.make(L=L, d=d, hidden=hid, ln_eps=cfg.ln_eps, n_mod=cfg.n_mod)
+    mbytes = h3.h3_mlp_workspace_size(mdesc)
+    mws = torch.empty(mbytes, dtype=torch.uint8, device=dev)
+    mout = torch.empty(L, d, dtype=torch.bfloat16, device=dev)
+    for _ in range(2):
+        h3.h3_mlp_block_fwd(mdesc, x, mod_d, shift, scale, gate, w1m, w2m, mws, mbytes, mout,
+                            stream=stream)
+    mev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    mev[0].record(stream)
+    for _ in range(5):
+        h3.h3_mlp_block_fwd(mdesc, x, mod_d, shift, scale, gate, w1m, w2m, mws, mbytes, mout,
+                            stream=stream)
+    mev[1].record(stream)
+    torch.cuda.synchronize(dev)
+    mlp_ms = mev[0].elapsed_time(mev[1]) / 5
+    mlp_flops = 4.0 * L * d * hid
+    del w1m, w2m, mws, mout
+
     # ---- one denoising-step update of the packed latent (C = 96 channels per
     # token: 24 latent channels x 1x2x2 patch), HBM-bound; L2 flushed between runs
     C_lat = 96
@@ -431,6 +454,9 @@ def run_gpu(args, cfg):
                                  "tflops": varlen_flops / (varlen_ms * 1e-3) / 1e12,
                                  "frac_of_sustained_bf16_peak":
                                      varlen_flops / (varlen_ms * 1e-3) / 1e12 / peak},
+        "mlp_block": {"hidden": hid, "ms": mlp_ms,
+                      "tflops": mlp_flops / (mlp_ms * 1e-3) / 1e12,
+                      "frac_of_sustained_bf16_peak": mlp_flops / (mlp_ms * 1e-3) / 1e12 / peak},
         "denoise_step": {"L": L, "C": C_lat, "ms": denoise_ms,
                          "gbs": denoise_bytes / (denoise_ms * 1e-3) / 1e9,
                          "frac_of_hbm_peak": denoise_bytes / (denoise_ms * 1e-3) / 1e9

@@ -84,6 +84,15 @@ typedef struct {
   const int32_t* cu_seqlens; /* host [n_seg + 1] when n_seg > 0 (see h3_joint_attn_varlen_fwd) */
 } h3_block_desc;
 
+/* Shape of one MLP sub-block (the feed-forward half of a DiT layer). */
+typedef struct {
+  int32_t L;            /* tokens, >= 1 */
+  int32_t d;            /* hidden size, d % 128 == 0 */
+  int32_t hidden;       /* feed-forward width (e.g. 4d), hidden % 128 == 0, <= 65536 */
+  float ln_eps;         /* LayerNorm epsilon (>= 0) */
+  int32_t n_mod;        /* rows of shift/scale/gate */
+} h3_mlp_desc;
+
 /* Largest number of segments a cu_seqlens array may describe. */
 #define H3_MAX_SEGMENTS 64
 
@@ -200,6 +209,24 @@ h3_status h3_denoise_step(float* z, float* x0, const uint16_t* v_h3, const uint8
                           const uint8_t* anchor, const float* z_anchor, int32_t L, int32_t C,
                           int32_t n_mod, const float* sigma, const float* sigma_next,
                           const uint8_t* update, h3_stream_t stream);
+
+/*
+ * The MLP sub-block that completes a DiT layer ([H3-RL]: feed-forward
+ * projections ff.net.0.proj and ff.net.2 next to the attention's to_q/k/v and
+ * to_out.0; modality-specific AdaLN branches; the pages give neither the
+ * width nor the activation: GELU, tanh form):
+ *   y   = LN(x) * (1 + scale[mod]) + shift[mod]
+ *   h   = gelu(y W1^T)                       W1 [hidden][d] bf16
+ *   out = x + gate[mod] * (h W2^T)           W2 [d][hidden] bf16
+ * Three launches on `stream`: modulate, up projection with the GELU in its
+ * epilogue, down projection with the gated residual in its epilogue.
+ * workspace >= h3_mlp_workspace_size() bytes, 256-byte aligned.  out may alias x.
+ */
+h3_status h3_mlp_workspace_size(const h3_mlp_desc* desc, size_t* bytes);
+h3_status h3_mlp_block_fwd(const h3_mlp_desc* desc, const uint16_t* x, const uint8_t* mod,
+                           const float* shift, const float* scale, const float* gate,
+                           const uint16_t* W1, const uint16_t* W2, void* workspace,
+                           size_t workspace_bytes, uint16_t* out, h3_stream_t stream);
 
 /* Bytes of device workspace h3_attn_block_fwd needs for `desc`. */
 h3_status h3_workspace_size(const h3_block_desc* desc, size_t* bytes);

@@ -22,7 +22,8 @@ __all__ = [
     "h3_workspace_size",
     "h3_attn_block_fwd", "h3_sync_status", "h3_set_wait_limit_ns",
     "h3_selftest_wait_timeout", "h3_attn_block_fwd_profiled", "h3_attn_block_fwd_noalloc",
-    "h3_denoise_step", "NOALLOC_SCRATCH_BYTES", "EXPORTED_SYMBOLS",
+    "h3_denoise_step", "MlpDesc", "h3_mlp_workspace_size", "h3_mlp_block_fwd",
+    "NOALLOC_SCRATCH_BYTES", "EXPORTED_SYMBOLS",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -38,7 +39,7 @@ EXPORTED_SYMBOLS = (
     "h3_out_proj_gated_residual",
     "h3_workspace_size", "h3_attn_block_fwd", "h3_sync_status", "h3_set_wait_limit_ns",
     "h3_selftest_wait_timeout", "h3_attn_block_fwd_profiled", "h3_attn_block_fwd_noalloc",
-    "h3_denoise_step",
+    "h3_denoise_step", "h3_mlp_workspace_size", "h3_mlp_block_fwd",
 )
 
 # Workspace the library keeps per GPU for h3_attn_block_fwd_noalloc.
@@ -68,6 +69,16 @@ class BlockDesc(ctypes.Structure):
                    0 if cu is None else len(cu) - 1, cu)
         desc._cu_keepalive = cu          # the struct points into this host array
         return desc
+
+
+class MlpDesc(ctypes.Structure):
+    _fields_ = [("L", ctypes.c_int32), ("d", ctypes.c_int32), ("hidden", ctypes.c_int32),
+                ("ln_eps", ctypes.c_float), ("n_mod", ctypes.c_int32)]
+
+    @classmethod
+    def make(cls, L, d, hidden=None, ln_eps=1e-6, n_mod=3) -> "MlpDesc":
+        return cls(int(L), int(d), int(4 * d if hidden is None else hidden), float(ln_eps),
+                   int(n_mod))
 
 
 def _int32_array(values):
@@ -100,6 +111,9 @@ def _sig(lib):
         [ctypes.POINTER(BlockDesc)] + [_P] * 9 + [ctypes.c_size_t, _P, _P, _P])
     lib.h3_attn_block_fwd_noalloc.argtypes = [ctypes.POINTER(BlockDesc)] + [_P] * 10
     lib.h3_denoise_step.argtypes = [_P] * 6 + [_I, _I, _I, _P, _P, _P, _P]
+    lib.h3_mlp_workspace_size.argtypes = [ctypes.POINTER(MlpDesc), ctypes.POINTER(ctypes.c_size_t)]
+    lib.h3_mlp_block_fwd.argtypes = [ctypes.POINTER(MlpDesc)] + [_P] * 8 + [ctypes.c_size_t, _P,
+                                                                            _P]
     lib.h3_sync_status.argtypes = [_P]
     lib.h3_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
     lib.h3_set_wait_limit_ns.restype = None
@@ -265,6 +279,21 @@ def h3_denoise_step(z, x0, v_h3, mod, anchor, z_anchor, L, C, sigma, sigma_next,
     _check("h3_denoise_step", load().h3_denoise_step(
         _addr(z), _addr(x0), _addr(v_h3), _addr(mod), _addr(anchor), _addr(z_anchor), L, C,
         n_mod, ctypes.addressof(sg), ctypes.addressof(sn), ctypes.addressof(up),
+        _stream(stream)))
+
+
+def h3_mlp_workspace_size(desc: MlpDesc) -> int:
+    n = ctypes.c_size_t(0)
+    _check("h3_mlp_workspace_size",
+           load().h3_mlp_workspace_size(ctypes.byref(desc), ctypes.byref(n)))
+    return int(n.value)
+
+
+def h3_mlp_block_fwd(desc: MlpDesc, x, mod, shift, scale, gate, W1, W2, workspace,
+                     workspace_bytes, out, stream=None) -> None:
+    _check("h3_mlp_block_fwd", load().h3_mlp_block_fwd(
+        ctypes.byref(desc), _addr(x), _addr(mod), _addr(shift), _addr(scale), _addr(gate),
+        _addr(W1), _addr(W2), _addr(workspace), int(workspace_bytes), _addr(out),
         _stream(stream)))
 
 

@@ -7,6 +7,8 @@
 //   EPI_GATED_RESIDUAL  C = x_res + gate[mod] * acc                 (output projection
 //                       + AdaLN gate; "DiffusionNFT on MiniMax H3", modality-specific
 //                       AdaLN branches)
+//   EPI_GELU            C = gelu(acc), tanh form                    (feed-forward up
+//                       projection ff.net.0.proj of the MLP sub-block)
 //
 // Layout of the work (one CTA per SM, 192 threads):
 //   warp 0      TMA producer: A tile 128x64 and B tile BNx64 per k-block into a
@@ -91,6 +93,14 @@ __device__ __forceinline__ void epilogue_chunk(const GemmDev& p, const RopeTable
         v[2 * j] = a * c - b * s;
         v[2 * j + 1] = a * s + b * c;
       }
+    }
+  }
+  if constexpr (EPI == EPI_GELU) {
+    // 0.5 u (1 + tanh(sqrt(2/pi) (u + 0.044715 u^3)))
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const float u = v[i];
+      v[i] = 0.5f * u * (1.f + tanhf(0.7978845608028654f * fmaf(0.044715f * u, u * u, u)));
     }
   }
   __nv_bfloat16* crow = p.C + size_t(grow) * p.N + gc;
@@ -328,6 +338,7 @@ cudaError_t launch_bn(const GemmArgs& a, const DevCtx& ctx, cudaStream_t st) {
     case EPI_PLAIN: return launch_typed<BN, EPI_PLAIN>(a, ctx, st);
     case EPI_ROPE: return launch_typed<BN, EPI_ROPE>(a, ctx, st);
     case EPI_GATED_RESIDUAL: return launch_typed<BN, EPI_GATED_RESIDUAL>(a, ctx, st);
+    case EPI_GELU: return launch_typed<BN, EPI_GELU>(a, ctx, st);
     default: return cudaErrorInvalidValue;
   }
 }

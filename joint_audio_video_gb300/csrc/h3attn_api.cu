@@ -289,6 +289,73 @@ h3_status h3_denoise_step(float* z, float* x0, const uint16_t* v_h3, const uint8
                                  reinterpret_cast<cudaStream_t>(stream)));
 }
 
+static h3_status check_mlp(const h3_mlp_desc* desc) {
+  if (desc == nullptr) return H3_ERR_INVALID_ARG;
+  if (desc->L < 1 || !valid_d(desc->d) || desc->n_mod < 1 || desc->n_mod > 255)
+    return H3_ERR_INVALID_ARG;
+  if (desc->hidden < 128 || desc->hidden % 128 != 0 || desc->hidden > 65536)
+    return H3_ERR_INVALID_ARG;
+  if (!(desc->ln_eps >= 0.f) || !std::isfinite(desc->ln_eps)) return H3_ERR_INVALID_ARG;
+  return H3_OK;
+}
+
+h3_status h3_mlp_workspace_size(const h3_mlp_desc* desc, size_t* bytes) {
+  if (bytes == nullptr) return H3_ERR_INVALID_ARG;
+  if (h3_status s = check_mlp(desc)) return s;
+  const size_t L = size_t(desc->L);
+  *bytes = round256(L * desc->d * 2) + round256(L * size_t(desc->hidden) * 2);
+  return H3_OK;
+}
+
+h3_status h3_mlp_block_fwd(const h3_mlp_desc* desc, const uint16_t* x, const uint8_t* mod,
+                           const float* shift, const float* scale, const float* gate,
+                           const uint16_t* W1, const uint16_t* W2, void* workspace,
+                           size_t workspace_bytes, uint16_t* out, h3_stream_t stream) {
+  size_t need = 0;
+  if (h3_status s = h3_mlp_workspace_size(desc, &need)) return s;
+  if (!aligned16(x) || mod == nullptr || !aligned16(shift) || !aligned16(scale) ||
+      !aligned16(gate) || !aligned16(W1) || !aligned16(W2) || !aligned16(out) ||
+      workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return H3_ERR_INVALID_ARG;
+  if (workspace_bytes < need) return H3_ERR_WORKSPACE;
+  const size_t L = size_t(desc->L), d = size_t(desc->d);
+  if (x != out && overlap(x, L * d * 2, out, L * d * 2)) return H3_ERR_INVALID_ARG;
+  if (overlap(workspace, need, x, L * d * 2) || overlap(workspace, need, out, L * d * 2))
+    return H3_ERR_INVALID_ARG;
+  DevCtx ctx;
+  if (h3_status s = dev_ctx(&ctx)) return s;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  void* y = ws;
+  void* hbuf = ws + round256(L * d * 2);
+  if (launch_adaln_modulate(x, mod, shift, scale, desc->L, desc->d, desc->n_mod, desc->ln_eps, y,
+                            ctx, st) != cudaSuccess)
+    return H3_ERR_CUDA;
+  GemmArgs up{};
+  up.A = y;
+  up.B = W1;
+  up.C = hbuf;
+  up.M = desc->L;
+  up.N = desc->hidden;
+  up.K = desc->d;
+  up.epilogue = EPI_GELU;
+  if (launch_gemm(up, ctx, st) != cudaSuccess) return H3_ERR_CUDA;
+  GemmArgs down{};
+  down.A = hbuf;
+  down.B = W2;
+  down.C = out;
+  down.M = desc->L;
+  down.N = desc->d;
+  down.K = desc->hidden;
+  down.epilogue = EPI_GATED_RESIDUAL;
+  down.x_res = x;
+  down.mod = mod;
+  down.gate = gate;
+  down.n_mod = desc->n_mod;
+  if (launch_gemm(down, ctx, st) != cudaSuccess) return H3_ERR_CUDA;
+  return H3_OK;
+}
+
 static h3_status check_desc(const h3_block_desc* desc) {
   if (desc == nullptr) return H3_ERR_INVALID_ARG;
   if (desc->L < 1 || desc->n_heads < 1 || desc->n_mod < 1 || desc->n_mod > 255)

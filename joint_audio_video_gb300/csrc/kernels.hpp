@@ -30,7 +30,7 @@ cudaError_t launch_adaln_modulate(const void* x, const uint8_t* mod, const float
 cudaError_t launch_mrope(void* qkv, const int32_t* pos, int L, int n_heads, const RopeTable& rt,
                          const DevCtx& ctx, cudaStream_t st);
 
-enum GemmEpilogue : int { EPI_PLAIN = 0, EPI_ROPE = 1, EPI_GATED_RESIDUAL = 2 };
+enum GemmEpilogue : int { EPI_PLAIN = 0, EPI_ROPE = 1, EPI_GATED_RESIDUAL = 2, EPI_GELU = 3 };
 
 struct GemmArgs {
   const void* A;        // [M][K] bf16, row-major

@@ -322,3 +322,28 @@ def denoise_step(z: np.ndarray, v_h3: np.ndarray, mod: np.ndarray, sigma, sigma_
         x0 = np.where(a, z_anchor, x0)
     return z_next, x0
 
+
+# ---------------------------------------------------------------------------
+# NEXT f3: the MLP sub-block that completes one DiT layer ([H3-RL] "How
+#   VeRL-Omni's Adapter Architecture Keeps H3-Specific Logic Contained": the
+#   feed-forward projections ff.net.0.proj and ff.net.2; modality-specific
+#   AdaLN branches).  Hidden width and activation are not given: 4d and the
+#   tanh form of GELU are readings (parity of those choices unpinned).
+# ---------------------------------------------------------------------------
+def gelu_tanh(u: np.ndarray) -> np.ndarray:
+    """GELU, tanh form: 0.5 u (1 + tanh(sqrt(2/pi) (u + 0.044715 u^3)))."""
+    return 0.5 * u * (1.0 + np.tanh(math.sqrt(2.0 / math.pi) * (u + 0.044715 * u ** 3)))
+
+
+def mlp_block(x: np.ndarray, mod: np.ndarray, shift: np.ndarray, scale: np.ndarray,
+              gate: np.ndarray, w1: np.ndarray, w2: np.ndarray, eps: float = 1e-6
+              ) -> Dict[str, np.ndarray]:
+    """out = x + gate[m] * (gelu(y W1^T) W2^T), y = LN(x)(1 + scale[m]) + shift[m].
+
+    ``w1 [hidden, d]`` (ff.net.0.proj), ``w2 [d, hidden]`` (ff.net.2).
+    """
+    y = adaln_modulate(x, mod, shift, scale, eps)
+    h = gelu_tanh(linear(y, w1))
+    branch = linear(h, w2)
+    return {"y": y, "h": h, "branch": branch, "out": gated_residual(x, branch, mod, gate)}
+

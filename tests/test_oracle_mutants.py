@@ -105,6 +105,11 @@ def _denoise_shared_schedule(z, v_h3, mod, sigma, sigma_next, update, anchor=Non
     return _ORIG["denoise_step"](z, v_h3, mod, s, sn, update, anchor, z_anchor)
 
 
+def _gelu_sigmoid_form(u):
+    """GELU by the sigmoid approximation u * sigmoid(1.702 u)."""
+    return u / (1.0 + np.exp(-1.702 * u))
+
+
 def _residual_wrong_index(x, branch, mod, gate):
     return x + gate[(mod.astype(np.int64) + 1) % 3] * branch
 
@@ -123,7 +128,7 @@ def _layout_audio_step_major(n_text, vt, vh, vw, ac, steps):
 _ORIG = {name: getattr(core, name) for name in
          ("layer_norm", "adaln_modulate", "linear", "rope_rotate_heads",
           "rope_angles", "attention", "attention_varlen", "gated_residual", "packed_layout",
-          "denoise_step")}
+          "denoise_step", "gelu_tanh")}
 
 MUTANTS = {
     "unbiased-variance": ("layer_norm", _ln_unbiased),
@@ -139,6 +144,7 @@ MUTANTS = {
     "varlen-boundary-off-by-one": ("attention_varlen", _varlen_boundary_off_by_one),
     "denoise-native-velocity-sign": ("denoise_step", _denoise_native_sign),
     "denoise-shared-schedule": ("denoise_step", _denoise_shared_schedule),
+    "gelu-sigmoid-form": ("gelu_tanh", _gelu_sigmoid_form),
 }
 
 PIN_TESTS = [getattr(pins, n) for n in dir(pins) if n.startswith("test_")]

@@ -458,3 +458,37 @@ def test_denoise_three_step_trace_reaches_clean_latents():
     free = (mod > 0) & ~anchor.astype(bool)
     np.testing.assert_allclose(z[free], x0[free], atol=1e-12)
     assert np.array_equal(z[mod == 0], eps[mod == 0])  # text rows never move
+
+
+# ------------------------------------------------------- MLP sub-block (NEXT f3)
+def test_gelu_identities_and_erf_form():
+    u = np.linspace(-6, 6, 241)
+    g = orc.gelu_tanh(u)
+    # odd part: gelu(u) - gelu(-u) = u exactly for the 0.5 u (1 + t(u)) form with odd t
+    np.testing.assert_allclose(g - orc.gelu_tanh(-u), u, atol=1e-13)
+    # the tanh form stays within 1e-3 of the exact erf form u * Phi(u)
+    exact = np.array([0.5 * v * (1 + math.erf(v / math.sqrt(2))) for v in u])
+    assert np.max(np.abs(g - exact)) < 1e-3
+    assert orc.gelu_tanh(np.array([0.0]))[0] == 0.0
+    assert abs(orc.gelu_tanh(np.array([30.0]))[0] - 30.0) < 1e-12
+    assert abs(orc.gelu_tanh(np.array([-30.0]))[0]) < 1e-12
+
+
+def test_mlp_block_reductions():
+    rng = np.random.default_rng(22)
+    L, d, hid = 6, 16, 64
+    x = rng.normal(size=(L, d))
+    mod = np.array([0, 1, 2, 2, 1, 0], dtype=np.uint8)
+    sh, sc, gt = (rng.normal(size=(3, d)) * 0.1 for _ in range(3))
+    w1 = rng.normal(size=(hid, d)) / 4
+    w2 = rng.normal(size=(d, hid)) / 8
+    r = orc.mlp_block(x, mod, sh, sc, gt, w1, w2)
+    assert np.array_equal(orc.mlp_block(x, mod, sh, sc, np.zeros((3, d)), w1, w2)["out"], x)
+    assert np.array_equal(orc.mlp_block(x, mod, sh, sc, gt, w1, np.zeros((d, hid)))["out"], x)
+    # brute-force one output element
+    y = orc.adaln_modulate(x, mod, sh, sc)
+    n, c = 3, 5
+    hrow = [0.5 * u * (1 + math.tanh(math.sqrt(2 / math.pi) * (u + 0.044715 * u ** 3)))
+            for u in (math.fsum(y[n, k] * w1[j, k] for k in range(d)) for j in range(hid))]
+    ref = x[n, c] + gt[mod[n], c] * math.fsum(hrow[j] * w2[c, j] for j in range(hid))
+    assert abs(r["out"][n, c] - ref) < 1e-12
