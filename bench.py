@@ -385,6 +385,55 @@ def run_gpu(args, cfg):
     mlp_flops = 4.0 * L * d * hid
     del w1m, w2m, mws, mout
 
+    # ---- the fp8 (E4M3) variants: both projections of the attention block and of
+    # the MLP in fp8 (weights quantised per output channel once, activations per
+    # token on every call); attention itself stays bf16
+    def quant(w):
+        q = torch.empty(w.shape, dtype=torch.uint8, device=dev)
+        sc8 = torch.empty(w.shape[0], dtype=torch.float32, device=dev)
+        h3.h3_quantize_rows_fp8(w, w.shape[0], w.shape[1], q, sc8, stream=stream)
+        return q, sc8
+
+    wqkv8, wqkv8s = quant(wqkv)
+    wo8, wo8s = quant(wo)
+    f8bytes = h3.h3_workspace_size_fp8(desc)
+    ws8 = torch.empty(f8bytes, dtype=torch.uint8, device=dev)
+    out8 = torch.empty(L, d, dtype=torch.bfloat16, device=dev)
+
+    def fp8_block():
+        h3.h3_attn_block_fwd_fp8(desc, x, mod_d, pos_d, shift, scale, gate, wqkv8, wqkv8s, wo8,
+                                 wo8s, ws8, f8bytes, out8, stream=stream)
+
+    def timed(fn, n=5):
+        fn()
+        ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ea.record(stream)
+        for _ in range(n):
+            fn()
+        eb.record(stream)
+        torch.cuda.synchronize(dev)
+        return ea.elapsed_time(eb) / n
+
+    fp8_block_ms = timed(fp8_block)
+    del ws8, out8, wqkv8, wo8
+    g8 = torch.Generator(device="cpu").manual_seed(11)
+    w1f = (torch.randn(4 * d, d, generator=g8) / d ** 0.5).to(torch.bfloat16).to(dev)
+    w2f = (torch.randn(d, 4 * d, generator=g8) / (4 * d) ** 0.5).to(torch.bfloat16).to(dev)
+    w1q, w1qs = quant(w1f)
+    w2q, w2qs = quant(w2f)
+    del w1f, w2f
+    m8desc = h3.MlpDesc.make(L=L, d=d, hidden=4 * d, ln_eps=cfg.ln_eps, n_mod=cfg.n_mod)
+    m8bytes = h3.h3_mlp_workspace_size_fp8(m8desc)
+    mws8 = torch.empty(m8bytes, dtype=torch.uint8, device=dev)
+    mout8 = torch.empty(L, d, dtype=torch.bfloat16, device=dev)
+    fp8_mlp_ms = timed(lambda: h3.h3_mlp_block_fwd_fp8(m8desc, x, mod_d, shift, scale, gate, w1q,
+                                                        w1qs, w2q, w2qs, mws8, m8bytes, mout8,
+                                                        stream=stream))
+    del mws8, mout8, w1q, w2q
+    st = h3.h3_sync_status(stream)
+    if st != 0:
+        raise RuntimeError(f"device status after the fp8 runs: {h3.h3_status_string(st)}")
+
     # ---- one denoising-step update of the packed latent (C = 96 channels per
     # token: 24 latent channels x 1x2x2 patch), HBM-bound; L2 flushed between runs
     C_lat = 96
@@ -457,6 +506,12 @@ def run_gpu(args, cfg):
         "mlp_block": {"hidden": hid, "ms": mlp_ms,
                       "tflops": mlp_flops / (mlp_ms * 1e-3) / 1e12,
                       "frac_of_sustained_bf16_peak": mlp_flops / (mlp_ms * 1e-3) / 1e12 / peak},
+        "fp8": {"attn_block_ms": fp8_block_ms,
+                "attn_block_tflops": cfg.flops() / (fp8_block_ms * 1e-3) / 1e12,
+                "mlp_block_ms": fp8_mlp_ms,
+                "mlp_block_tflops": mlp_flops / (fp8_mlp_ms * 1e-3) / 1e12,
+                "note": "projections in E4M3 (tcgen05 kind::f8f6f4), attention bf16; FLOPs "
+                        "counted as for the bf16 block"},
         "denoise_step": {"L": L, "C": C_lat, "ms": denoise_ms,
                          "gbs": denoise_bytes / (denoise_ms * 1e-3) / 1e9,
                          "frac_of_hbm_peak": denoise_bytes / (denoise_ms * 1e-3) / 1e9

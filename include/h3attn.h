@@ -228,6 +228,54 @@ h3_status h3_mlp_block_fwd(const h3_mlp_desc* desc, const uint16_t* x, const uin
                            const uint16_t* W1, const uint16_t* W2, void* workspace,
                            size_t workspace_bytes, uint16_t* out, h3_stream_t stream);
 
+/*
+ * FP8 (E4M3) variant of the projections ([vLLM] §5 Distributed Layerwise
+ * Offload: the active block held at FP8 -- prior art; the oracle is the same
+ * fp64 block, the tolerance follows from the E4M3 unit roundoff 2^-4).
+ *
+ * Row-wise quantisation: scale[r] = max|x[r]| / 448 (1 for an all-zero row),
+ * q[r][k] = E4M3(x[r][k] / scale[r]), round-to-nearest, saturating.
+ *   x [R][K] bf16 -> q [R][K] bytes, scale [R] fp32; K % 16 == 0.
+ * Used on activations (one scale per token) and on weights (one scale per
+ * output channel: the rows of W[out][in]).
+ */
+h3_status h3_quantize_rows_fp8(const uint16_t* x, int32_t R, int32_t K, uint8_t* q, float* scale,
+                               h3_stream_t stream);
+
+/*
+ * C[m][n] = a_scale[m] * b_scale[n] * sum_k A[m][k] B[n][k] with E4M3 A [M][K]
+ * and B [N][K] (tcgen05 kind::f8f6f4, fp32 accumulation) -> C [M][N] bf16.
+ * N % 128 == 0, K % 128 == 0.
+ */
+h3_status h3_gemm_fp8(const uint8_t* A, const float* a_scale, const uint8_t* B,
+                      const float* b_scale, int32_t M, int32_t N, int32_t K, uint16_t* C,
+                      h3_stream_t stream);
+
+/*
+ * h3_attn_block_fwd with the two projections in FP8: y and O are quantised
+ * per token before the QKV projection (RoPE in its epilogue) and the output
+ * projection (gated residual in its epilogue); attention stays bf16.
+ *   Wqkv_q [3d][d], Wo_q [d][d]: E4M3 weights from h3_quantize_rows_fp8, with
+ *   their per-output-channel scales Wqkv_s [3d], Wo_s [d].
+ * workspace >= h3_workspace_size_fp8(desc) bytes, 256-byte aligned.
+ */
+h3_status h3_workspace_size_fp8(const h3_block_desc* desc, size_t* bytes);
+h3_status h3_attn_block_fwd_fp8(const h3_block_desc* desc, const uint16_t* x, const uint8_t* mod,
+                                const int32_t* pos, const float* shift, const float* scale,
+                                const float* gate, const uint8_t* Wqkv_q, const float* Wqkv_s,
+                                const uint8_t* Wo_q, const float* Wo_s, void* workspace,
+                                size_t workspace_bytes, uint16_t* out, h3_stream_t stream);
+
+/* h3_mlp_block_fwd with both feed-forward projections in FP8 (y and h
+ * quantised per token; W1_q [hidden][d], W2_q [d][hidden] with per-output-
+ * channel scales W1_s [hidden], W2_s [d]). */
+h3_status h3_mlp_workspace_size_fp8(const h3_mlp_desc* desc, size_t* bytes);
+h3_status h3_mlp_block_fwd_fp8(const h3_mlp_desc* desc, const uint16_t* x, const uint8_t* mod,
+                               const float* shift, const float* scale, const float* gate,
+                               const uint8_t* W1_q, const float* W1_s, const uint8_t* W2_q,
+                               const float* W2_s, void* workspace, size_t workspace_bytes,
+                               uint16_t* out, h3_stream_t stream);
+
 /* Bytes of device workspace h3_attn_block_fwd needs for `desc`. */
 h3_status h3_workspace_size(const h3_block_desc* desc, size_t* bytes);
 

@@ -23,6 +23,8 @@ __all__ = [
     "h3_attn_block_fwd", "h3_sync_status", "h3_set_wait_limit_ns",
     "h3_selftest_wait_timeout", "h3_attn_block_fwd_profiled", "h3_attn_block_fwd_noalloc",
     "h3_denoise_step", "MlpDesc", "h3_mlp_workspace_size", "h3_mlp_block_fwd",
+    "h3_quantize_rows_fp8", "h3_gemm_fp8", "h3_workspace_size_fp8", "h3_attn_block_fwd_fp8",
+    "h3_mlp_workspace_size_fp8", "h3_mlp_block_fwd_fp8",
     "NOALLOC_SCRATCH_BYTES", "EXPORTED_SYMBOLS",
 ]
 
@@ -40,6 +42,8 @@ EXPORTED_SYMBOLS = (
     "h3_workspace_size", "h3_attn_block_fwd", "h3_sync_status", "h3_set_wait_limit_ns",
     "h3_selftest_wait_timeout", "h3_attn_block_fwd_profiled", "h3_attn_block_fwd_noalloc",
     "h3_denoise_step", "h3_mlp_workspace_size", "h3_mlp_block_fwd",
+    "h3_quantize_rows_fp8", "h3_gemm_fp8", "h3_workspace_size_fp8", "h3_attn_block_fwd_fp8",
+    "h3_mlp_workspace_size_fp8", "h3_mlp_block_fwd_fp8",
 )
 
 # Workspace the library keeps per GPU for h3_attn_block_fwd_noalloc.
@@ -114,6 +118,15 @@ def _sig(lib):
     lib.h3_mlp_workspace_size.argtypes = [ctypes.POINTER(MlpDesc), ctypes.POINTER(ctypes.c_size_t)]
     lib.h3_mlp_block_fwd.argtypes = [ctypes.POINTER(MlpDesc)] + [_P] * 8 + [ctypes.c_size_t, _P,
                                                                             _P]
+    lib.h3_quantize_rows_fp8.argtypes = [_P, _I, _I, _P, _P, _P]
+    lib.h3_gemm_fp8.argtypes = [_P, _P, _P, _P, _I, _I, _I, _P, _P]
+    lib.h3_workspace_size_fp8.argtypes = [ctypes.POINTER(BlockDesc), ctypes.POINTER(ctypes.c_size_t)]
+    lib.h3_attn_block_fwd_fp8.argtypes = ([ctypes.POINTER(BlockDesc)] + [_P] * 11 +
+                                          [ctypes.c_size_t, _P, _P])
+    lib.h3_mlp_workspace_size_fp8.argtypes = [ctypes.POINTER(MlpDesc),
+                                              ctypes.POINTER(ctypes.c_size_t)]
+    lib.h3_mlp_block_fwd_fp8.argtypes = ([ctypes.POINTER(MlpDesc)] + [_P] * 10 +
+                                         [ctypes.c_size_t, _P, _P])
     lib.h3_sync_status.argtypes = [_P]
     lib.h3_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
     lib.h3_set_wait_limit_ns.restype = None
@@ -295,6 +308,46 @@ def h3_mlp_block_fwd(desc: MlpDesc, x, mod, shift, scale, gate, W1, W2, workspac
         ctypes.byref(desc), _addr(x), _addr(mod), _addr(shift), _addr(scale), _addr(gate),
         _addr(W1), _addr(W2), _addr(workspace), int(workspace_bytes), _addr(out),
         _stream(stream)))
+
+
+def h3_quantize_rows_fp8(x, R, K, q, scale, stream=None) -> None:
+    _check("h3_quantize_rows_fp8", load().h3_quantize_rows_fp8(
+        _addr(x), R, K, _addr(q), _addr(scale), _stream(stream)))
+
+
+def h3_gemm_fp8(A, a_scale, B, b_scale, M, N, K, C, stream=None) -> None:
+    _check("h3_gemm_fp8", load().h3_gemm_fp8(_addr(A), _addr(a_scale), _addr(B), _addr(b_scale),
+                                             M, N, K, _addr(C), _stream(stream)))
+
+
+def h3_workspace_size_fp8(desc: BlockDesc) -> int:
+    n = ctypes.c_size_t(0)
+    _check("h3_workspace_size_fp8",
+           load().h3_workspace_size_fp8(ctypes.byref(desc), ctypes.byref(n)))
+    return int(n.value)
+
+
+def h3_attn_block_fwd_fp8(desc: BlockDesc, x, mod, pos, shift, scale, gate, Wqkv_q, Wqkv_s,
+                          Wo_q, Wo_s, workspace, workspace_bytes, out, stream=None) -> None:
+    _check("h3_attn_block_fwd_fp8", load().h3_attn_block_fwd_fp8(
+        ctypes.byref(desc), _addr(x), _addr(mod), _addr(pos), _addr(shift), _addr(scale),
+        _addr(gate), _addr(Wqkv_q), _addr(Wqkv_s), _addr(Wo_q), _addr(Wo_s), _addr(workspace),
+        int(workspace_bytes), _addr(out), _stream(stream)))
+
+
+def h3_mlp_workspace_size_fp8(desc: MlpDesc) -> int:
+    n = ctypes.c_size_t(0)
+    _check("h3_mlp_workspace_size_fp8",
+           load().h3_mlp_workspace_size_fp8(ctypes.byref(desc), ctypes.byref(n)))
+    return int(n.value)
+
+
+def h3_mlp_block_fwd_fp8(desc: MlpDesc, x, mod, shift, scale, gate, W1_q, W1_s, W2_q, W2_s,
+                         workspace, workspace_bytes, out, stream=None) -> None:
+    _check("h3_mlp_block_fwd_fp8", load().h3_mlp_block_fwd_fp8(
+        ctypes.byref(desc), _addr(x), _addr(mod), _addr(shift), _addr(scale), _addr(gate),
+        _addr(W1_q), _addr(W1_s), _addr(W2_q), _addr(W2_s), _addr(workspace),
+        int(workspace_bytes), _addr(out), _stream(stream)))
 
 
 def h3_sync_status(stream=None) -> int:

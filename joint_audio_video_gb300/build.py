@@ -25,7 +25,7 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CUFLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
            "-Xptxas", "-v", "-I", INCLUDE, "-I", CSRC]
 SOURCES = ["h3attn_api.cu", "adaln.cu", "mrope.cu", "gemm.cu", "attn.cu", "layout.cpp",
-           "noalloc.cu", "denoise.cu"]
+           "noalloc.cu", "denoise.cu", "quant.cu"]
 HEADERS = ["ptx.cuh", "tmap.hpp", "kernels.hpp"]
 
 

@@ -1,5 +1,6 @@
-// Persistent tcgen05 GEMM  C[M][N] = A[M][K] * B[N][K]^T  (bf16 in, fp32 accumulate)
-// with the sub-block's fused epilogues:
+// Persistent tcgen05 GEMM  C[M][N] = A[M][K] * B[N][K]^T  (bf16 or fp8 E4M3 in,
+// fp32 accumulate; fp8 results are scaled by a_scale[row] * b_scale[col]) with the
+// sub-block's fused epilogues:
 //   EPI_PLAIN           C = acc                                     (h3_qkv_proj)
 //   EPI_ROPE            Q/K columns rotated by the 3D (t,h,w) RoPE, V as is
 //                       (fused QKV projection of the block; "Joint Audio-Video
@@ -31,7 +32,7 @@ namespace h3 {
 namespace {
 
 constexpr int BM = 128;
-constexpr int BK = 64;
+constexpr int BK = 64;          // bf16 elements per k-block (128 bytes; fp8: 128 elements)
 constexpr int kThreads = 192;
 constexpr int kGroupM = 16;
 
@@ -57,6 +58,8 @@ struct GemmDev {
   int n_mod;
   int* status;
   uint64_t wait_ns;
+  const float* a_scale;
+  const float* b_scale;
 };
 
 __device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int& mb, int& nb) {
@@ -71,13 +74,24 @@ __device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int& mb
 
 // Epilogue of one 32-column chunk held in r[] (fp32 bits) for row `grow`,
 // global columns gc .. gc+31.
-template <int EPI>
+template <int EPI, bool FP8>
 __device__ __forceinline__ void epilogue_chunk(const GemmDev& p, const RopeTable& rt,
                                                uint32_t (&r)[32], int grow, int gc,
-                                               const int32_t (&pr)[3], int m) {
+                                               const int32_t (&pr)[3], int m, float sa) {
   float v[32];
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+  if constexpr (FP8) {   // dequantise: row scale of A times column scale of B
+    const float4* sb = reinterpret_cast<const float4*>(p.b_scale + gc);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float4 b = __ldg(sb + i);
+      v[4 * i + 0] *= sa * b.x;
+      v[4 * i + 1] *= sa * b.y;
+      v[4 * i + 2] *= sa * b.z;
+      v[4 * i + 3] *= sa * b.w;
+    }
+  }
   if constexpr (EPI == EPI_ROPE) {
     if (gc < 2 * p.d) {   // Q or K block: rotate pairs (2k, 2k+1) of the head
       const int k0 = (gc & 127) >> 1;
@@ -129,7 +143,7 @@ __device__ __forceinline__ void epilogue_chunk(const GemmDev& p, const RopeTable
   }
 }
 
-template <int BN, int EPI>
+template <int BN, int EPI, bool FP8>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ GemmDev p, const __grid_constant__ RopeTable rt) {
@@ -171,7 +185,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = tmem_base_sh;
 
   const int num_tiles = p.num_m * p.num_n;
-  const int kblocks = p.K / BK;
+  const int kblocks = FP8 ? p.K / (2 * BK) : p.K / BK;   // 128-byte k-blocks
 
   if (warp == 0) {
     // ---------------------------------------------------------------- producer
@@ -187,8 +201,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t fb = smem_u32(&bar_full[stage]);
           const uint32_t sa = base + stage * Cfg::kStageBytes;
           mbar_arrive_expect_tx(fb, Cfg::kStageBytes);
-          tma_load_2d(sa, &tmA, fb, kb * BK, mb * BM);
-          tma_load_2d(sa + Cfg::kABytes, &tmB, fb, kb * BK, nb * BN);
+          const int kx = FP8 ? kb * 2 * BK : kb * BK;   // element coordinate of the k-block
+          tma_load_2d(sa, &tmA, fb, kx, mb * BM);
+          tma_load_2d(sa + Cfg::kABytes, &tmB, fb, kx, nb * BN);
           if (++stage == S) { stage = 0; phase ^= 1u; }
         }
       }
@@ -207,7 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane_id() == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, 0, 0);
+      constexpr uint32_t idesc = FP8 ? idesc_e4m3_f32(BM, BN) : idesc_bf16_f32(BM, BN, 0, 0);
       // stages are kStageBytes apart: precomputed descriptors plus one add per MMA
       const SDesc dA0 = sdesc_split(sdesc_sw128(base, 16, 1024));
       const SDesc dB0 = sdesc_split(sdesc_sw128(base + Cfg::kABytes, 16, 1024));
@@ -226,9 +241,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const uint32_t soff = stage * (Cfg::kStageBytes >> 4);
           const SDesc dA{dA0.lo + soff, dA0.hi}, dB{dB0.lo + soff, dB0.hi};
+          // 4 steps of 32 bytes along K: K=16 for bf16, K=32 for fp8
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k)
-            mma_bf16_ss(dtm, sdesc_at(dA, k * 32), sdesc_at(dB, k * 32), idesc, (kb | k) != 0);
+          for (int k = 0; k < 4; ++k) {
+            if constexpr (FP8)
+              mma_f8_ss(dtm, sdesc_at(dA, k * 32), sdesc_at(dB, k * 32), idesc, (kb | k) != 0);
+            else
+              mma_bf16_ss(dtm, sdesc_at(dA, k * 32), sdesc_at(dB, k * 32), idesc, (kb | k) != 0);
+          }
           tc_commit(smem_u32(&bar_empty[stage]));
           if (++stage == S) { stage = 0; phase ^= 1u; }
         }
@@ -266,6 +286,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           pr[2] = p.pos[size_t(grow) * 3 + 2];
         }
       }
+      float sa = 1.f;
+      if constexpr (FP8) {
+        if (live) sa = __ldg(p.a_scale + grow);
+      }
       bool bad = false;
       if constexpr (EPI == EPI_GATED_RESIDUAL) {
         if (live) {
@@ -284,7 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < 32; ++i) r[i] = 0x7FC00000u;   // NaN row
           }
-          epilogue_chunk<EPI>(p, rt, r, grow, nb * BN + c * 32, pr, m);
+          epilogue_chunk<EPI, FP8>(p, rt, r, grow, nb * BN + c * 32, pr, m, sa);
         }
       }
       if (bad) atomicCAS(p.status, H3_DEV_OK, H3_DEV_BAD_INDEX);
@@ -299,12 +323,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, Cfg::kTmemCols);
 }
 
-template <int BN, int EPI>
+template <int BN, int EPI, bool FP8>
 cudaError_t launch_typed(const GemmArgs& a, const DevCtx& ctx, cudaStream_t st) {
   using Cfg = GemmCfg<BN>;
   CUtensorMap tmA, tmB;
-  if (!make_tmap_bf16_2d(&tmA, a.A, a.M, a.K, a.K, BM, BK)) return cudaErrorInvalidValue;
-  if (!make_tmap_bf16_2d(&tmB, a.B, a.N, a.K, a.K, BN, BK)) return cudaErrorInvalidValue;
+  if constexpr (FP8) {
+    if (!make_tmap_u8_2d(&tmA, a.A, a.M, a.K, a.K, BM)) return cudaErrorInvalidValue;
+    if (!make_tmap_u8_2d(&tmB, a.B, a.N, a.K, a.K, BN)) return cudaErrorInvalidValue;
+  } else {
+    if (!make_tmap_bf16_2d(&tmA, a.A, a.M, a.K, a.K, BM, BK)) return cudaErrorInvalidValue;
+    if (!make_tmap_bf16_2d(&tmB, a.B, a.N, a.K, a.K, BN, BK)) return cudaErrorInvalidValue;
+  }
   GemmDev p{};
   p.C = static_cast<__nv_bfloat16*>(a.C);
   p.M = a.M;
@@ -320,9 +349,11 @@ cudaError_t launch_typed(const GemmArgs& a, const DevCtx& ctx, cudaStream_t st) 
   p.n_mod = a.n_mod;
   p.status = ctx.status;
   p.wait_ns = ctx.wait_ns;
+  p.a_scale = a.a_scale;
+  p.b_scale = a.b_scale;
   RopeTable rt{};
   if (a.rope) rt = *a.rope;
-  auto kern = gemm_kernel<BN, EPI>;
+  auto kern = gemm_kernel<BN, EPI, FP8>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        int(Cfg::kSmem));
   if (e != cudaSuccess) return e;
@@ -332,13 +363,13 @@ cudaError_t launch_typed(const GemmArgs& a, const DevCtx& ctx, cudaStream_t st) 
   return cudaGetLastError();
 }
 
-template <int BN>
+template <int BN, bool FP8>
 cudaError_t launch_bn(const GemmArgs& a, const DevCtx& ctx, cudaStream_t st) {
   switch (a.epilogue) {
-    case EPI_PLAIN: return launch_typed<BN, EPI_PLAIN>(a, ctx, st);
-    case EPI_ROPE: return launch_typed<BN, EPI_ROPE>(a, ctx, st);
-    case EPI_GATED_RESIDUAL: return launch_typed<BN, EPI_GATED_RESIDUAL>(a, ctx, st);
-    case EPI_GELU: return launch_typed<BN, EPI_GELU>(a, ctx, st);
+    case EPI_PLAIN: return launch_typed<BN, EPI_PLAIN, FP8>(a, ctx, st);
+    case EPI_ROPE: return launch_typed<BN, EPI_ROPE, FP8>(a, ctx, st);
+    case EPI_GATED_RESIDUAL: return launch_typed<BN, EPI_GATED_RESIDUAL, FP8>(a, ctx, st);
+    case EPI_GELU: return launch_typed<BN, EPI_GELU, FP8>(a, ctx, st);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -346,8 +377,12 @@ cudaError_t launch_bn(const GemmArgs& a, const DevCtx& ctx, cudaStream_t st) {
 }  // namespace
 
 cudaError_t launch_gemm(const GemmArgs& a, const DevCtx& ctx, cudaStream_t st) {
-  if (a.N % 256 == 0) return launch_bn<256>(a, ctx, st);
-  return launch_bn<128>(a, ctx, st);
+  if (a.fp8) {
+    if (a.N % 256 == 0) return launch_bn<256, true>(a, ctx, st);
+    return launch_bn<128, true>(a, ctx, st);
+  }
+  if (a.N % 256 == 0) return launch_bn<256, false>(a, ctx, st);
+  return launch_bn<128, false>(a, ctx, st);
 }
 
 }  // namespace h3

@@ -356,6 +356,199 @@ h3_status h3_mlp_block_fwd(const h3_mlp_desc* desc, const uint16_t* x, const uin
   return H3_OK;
 }
 
+h3_status h3_quantize_rows_fp8(const uint16_t* x, int32_t R, int32_t K, uint8_t* q, float* scale,
+                               h3_stream_t stream) {
+  if (R < 1 || K < 16 || K % 16 != 0) return H3_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(q) || scale == nullptr ||
+      (reinterpret_cast<uintptr_t>(scale) & 3u))
+    return H3_ERR_INVALID_ARG;
+  DevCtx ctx;
+  if (h3_status s = dev_ctx(&ctx)) return s;
+  return launched(launch_quantize_rows(x, R, K, q, scale, ctx,
+                                       reinterpret_cast<cudaStream_t>(stream)));
+}
+
+h3_status h3_gemm_fp8(const uint8_t* A, const float* a_scale, const uint8_t* B,
+                      const float* b_scale, int32_t M, int32_t N, int32_t K, uint16_t* C,
+                      h3_stream_t stream) {
+  if (M < 1 || N < 128 || N % 128 != 0 || K < 128 || K % 128 != 0) return H3_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(B) || !aligned16(C) || !aligned16(a_scale) ||
+      !aligned16(b_scale))
+    return H3_ERR_INVALID_ARG;
+  DevCtx ctx;
+  if (h3_status s = dev_ctx(&ctx)) return s;
+  GemmArgs g{};
+  g.A = A;
+  g.B = B;
+  g.C = C;
+  g.M = M;
+  g.N = N;
+  g.K = K;
+  g.epilogue = EPI_PLAIN;
+  g.fp8 = 1;
+  g.a_scale = a_scale;
+  g.b_scale = b_scale;
+  return launched(launch_gemm(g, ctx, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+static h3_status check_desc(const h3_block_desc* desc);
+
+h3_status h3_workspace_size_fp8(const h3_block_desc* desc, size_t* bytes) {
+  if (bytes == nullptr) return H3_ERR_INVALID_ARG;
+  if (h3_status s = check_desc(desc)) return s;
+  const size_t L = size_t(desc->L), d = size_t(desc->d);
+  *bytes = round256(L * d * 2) + round256(L * 3 * d * 2) + round256(L * d) + round256(L * 4);
+  return H3_OK;
+}
+
+h3_status h3_attn_block_fwd_fp8(const h3_block_desc* desc, const uint16_t* x, const uint8_t* mod,
+                                const int32_t* pos, const float* shift, const float* scale,
+                                const float* gate, const uint8_t* Wqkv_q, const float* Wqkv_s,
+                                const uint8_t* Wo_q, const float* Wo_s, void* workspace,
+                                size_t workspace_bytes, uint16_t* out, h3_stream_t stream) {
+  size_t need = 0;
+  if (h3_status s = h3_workspace_size_fp8(desc, &need)) return s;
+  if (!aligned16(x) || mod == nullptr || pos == nullptr || (reinterpret_cast<uintptr_t>(pos) & 3u) ||
+      !aligned16(shift) || !aligned16(scale) || !aligned16(gate) || !aligned16(Wqkv_q) ||
+      !aligned16(Wqkv_s) || !aligned16(Wo_q) || !aligned16(Wo_s) || !aligned16(out) ||
+      workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return H3_ERR_INVALID_ARG;
+  if (workspace_bytes < need) return H3_ERR_WORKSPACE;
+  const size_t L = size_t(desc->L), d = size_t(desc->d);
+  if (x != out && overlap(x, L * d * 2, out, L * d * 2)) return H3_ERR_INVALID_ARG;
+  if (overlap(workspace, need, x, L * d * 2) || overlap(workspace, need, out, L * d * 2))
+    return H3_ERR_INVALID_ARG;
+  DevCtx ctx;
+  if (h3_status s = dev_ctx(&ctx)) return s;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  void* y = ws;                                        // y, then O
+  void* qkv = ws + round256(L * d * 2);
+  void* q8 = ws + round256(L * d * 2) + round256(L * 3 * d * 2);
+  float* s8 = reinterpret_cast<float*>(static_cast<uint8_t*>(q8) + round256(L * d));
+  const int Li = desc->L, di = desc->d;
+  if (launch_adaln_modulate(x, mod, shift, scale, Li, di, desc->n_mod, desc->ln_eps, y, ctx, st) !=
+          cudaSuccess ||
+      launch_quantize_rows(y, Li, di, q8, s8, ctx, st) != cudaSuccess)
+    return H3_ERR_CUDA;
+  RopeTable rt;
+  make_rope_table(&rt, desc->rope_sec, desc->rope_base);
+  GemmArgs g{};
+  g.A = q8;
+  g.B = Wqkv_q;
+  g.C = qkv;
+  g.M = Li;
+  g.N = 3 * di;
+  g.K = di;
+  g.epilogue = EPI_ROPE;
+  g.pos = pos;
+  g.d = di;
+  g.rope = &rt;
+  g.fp8 = 1;
+  g.a_scale = s8;
+  g.b_scale = Wqkv_s;
+  if (launch_gemm(g, ctx, st) != cudaSuccess) return H3_ERR_CUDA;
+  AttnArgs a{};
+  a.qkv = qkv;
+  a.O = y;
+  a.L = Li;
+  a.H = desc->n_heads;
+  a.causal = desc->causal;
+  a.sm_scale = 1.0f / std::sqrt(float(desc->head_dim));
+  a.n_seg = desc->n_seg;
+  a.cu_seqlens = desc->cu_seqlens;
+  if (launch_attention(a, ctx, st) != cudaSuccess ||
+      launch_quantize_rows(y, Li, di, q8, s8, ctx, st) != cudaSuccess)
+    return H3_ERR_CUDA;
+  GemmArgs o{};
+  o.A = q8;
+  o.B = Wo_q;
+  o.C = out;
+  o.M = Li;
+  o.N = di;
+  o.K = di;
+  o.epilogue = EPI_GATED_RESIDUAL;
+  o.x_res = x;
+  o.mod = mod;
+  o.gate = gate;
+  o.n_mod = desc->n_mod;
+  o.fp8 = 1;
+  o.a_scale = s8;
+  o.b_scale = Wo_s;
+  return launched(launch_gemm(o, ctx, st));
+}
+
+static h3_status check_mlp(const h3_mlp_desc* desc);
+
+h3_status h3_mlp_workspace_size_fp8(const h3_mlp_desc* desc, size_t* bytes) {
+  if (bytes == nullptr) return H3_ERR_INVALID_ARG;
+  if (h3_status s = check_mlp(desc)) return s;
+  const size_t L = size_t(desc->L), d = size_t(desc->d), hid = size_t(desc->hidden);
+  *bytes = round256(L * d * 2) + round256(L * hid * 2) + round256(L * hid) + round256(L * 4);
+  return H3_OK;
+}
+
+h3_status h3_mlp_block_fwd_fp8(const h3_mlp_desc* desc, const uint16_t* x, const uint8_t* mod,
+                               const float* shift, const float* scale, const float* gate,
+                               const uint8_t* W1_q, const float* W1_s, const uint8_t* W2_q,
+                               const float* W2_s, void* workspace, size_t workspace_bytes,
+                               uint16_t* out, h3_stream_t stream) {
+  size_t need = 0;
+  if (h3_status s = h3_mlp_workspace_size_fp8(desc, &need)) return s;
+  if (!aligned16(x) || mod == nullptr || !aligned16(shift) || !aligned16(scale) ||
+      !aligned16(gate) || !aligned16(W1_q) || !aligned16(W1_s) || !aligned16(W2_q) ||
+      !aligned16(W2_s) || !aligned16(out) || workspace == nullptr ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return H3_ERR_INVALID_ARG;
+  if (workspace_bytes < need) return H3_ERR_WORKSPACE;
+  const size_t L = size_t(desc->L), d = size_t(desc->d), hid = size_t(desc->hidden);
+  if (x != out && overlap(x, L * d * 2, out, L * d * 2)) return H3_ERR_INVALID_ARG;
+  if (overlap(workspace, need, x, L * d * 2) || overlap(workspace, need, out, L * d * 2))
+    return H3_ERR_INVALID_ARG;
+  DevCtx ctx;
+  if (h3_status s = dev_ctx(&ctx)) return s;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  void* y = ws;
+  void* hbuf = ws + round256(L * d * 2);
+  void* q8 = static_cast<uint8_t*>(hbuf) + round256(L * hid * 2);   // y_q, later h_q
+  float* s8 = reinterpret_cast<float*>(static_cast<uint8_t*>(q8) + round256(L * hid));
+  if (launch_adaln_modulate(x, mod, shift, scale, desc->L, desc->d, desc->n_mod, desc->ln_eps, y,
+                            ctx, st) != cudaSuccess ||
+      launch_quantize_rows(y, desc->L, desc->d, q8, s8, ctx, st) != cudaSuccess)
+    return H3_ERR_CUDA;
+  GemmArgs up{};
+  up.A = q8;
+  up.B = W1_q;
+  up.C = hbuf;
+  up.M = desc->L;
+  up.N = desc->hidden;
+  up.K = desc->d;
+  up.epilogue = EPI_GELU;
+  up.fp8 = 1;
+  up.a_scale = s8;
+  up.b_scale = W1_s;
+  if (launch_gemm(up, ctx, st) != cudaSuccess ||
+      launch_quantize_rows(hbuf, desc->L, desc->hidden, q8, s8, ctx, st) != cudaSuccess)
+    return H3_ERR_CUDA;
+  GemmArgs down{};
+  down.A = q8;
+  down.B = W2_q;
+  down.C = out;
+  down.M = desc->L;
+  down.N = desc->d;
+  down.K = desc->hidden;
+  down.epilogue = EPI_GATED_RESIDUAL;
+  down.x_res = x;
+  down.mod = mod;
+  down.gate = gate;
+  down.n_mod = desc->n_mod;
+  down.fp8 = 1;
+  down.a_scale = s8;
+  down.b_scale = W2_s;
+  return launched(launch_gemm(down, ctx, st));
+}
+
 static h3_status check_desc(const h3_block_desc* desc) {
   if (desc == nullptr) return H3_ERR_INVALID_ARG;
   if (desc->L < 1 || desc->n_heads < 1 || desc->n_mod < 1 || desc->n_mod > 255)

@@ -47,6 +47,10 @@ struct GemmArgs {
   const uint8_t* mod;   // [M]
   const float* gate;    // [n_mod][N]
   int n_mod;
+  // fp8 operands: A and B are E4M3 bytes; acc is scaled by a_scale[row] * b_scale[col]
+  int fp8;
+  const float* a_scale; // [M]
+  const float* b_scale; // [N]
 };
 
 cudaError_t launch_gemm(const GemmArgs& a, const DevCtx& ctx, cudaStream_t st);
@@ -65,6 +69,10 @@ struct AttnArgs {
 };
 
 cudaError_t launch_attention(const AttnArgs& a, const DevCtx& ctx, cudaStream_t st);
+
+// Row-wise E4M3 quantisation: q[r] = RN(x[r] / s[r]) with s[r] = max|x[r]| / 448.
+cudaError_t launch_quantize_rows(const void* x, int R, int K, void* q, float* scale,
+                                 const DevCtx& ctx, cudaStream_t st);
 
 // Per-modality noise levels of one denoising step (host-validated).
 struct DenoiseParams {

@@ -30,7 +30,7 @@ def _declared():
 
 def test_library_exports_every_declared_entry_point(lib):
     names = _declared()
-    assert len(names) == 19, names
+    assert len(names) == 25, names
     raw = ctypes.CDLL(lib.lib_path)
     for n in names:
         assert hasattr(raw, n), f"{n} declared but not exported"
@@ -177,3 +177,16 @@ def test_denoise_arguments_are_validated_before_launch(lib):
                              a(up), None) == 1               # misaligned state
     assert L.h3_denoise_step(p, p + 16, p + (1 << 24), p, None, None, 10, 8, 3, a(s3), a(s3),
                              a(up), None) == 1               # x0 overlapping z
+
+
+def test_fp8_arguments_are_validated_before_launch(lib):
+    L = lib.load()
+    p = 1 << 20
+    assert L.h3_quantize_rows_fp8(p, 4, 24, p + (1 << 24), p + (1 << 25), None) == 1   # K % 16
+    assert L.h3_quantize_rows_fp8(p, 0, 32, p + (1 << 24), p + (1 << 25), None) == 1   # R < 1
+    assert L.h3_gemm_fp8(p, p, p, p, 8, 200, 256, p, None) == 1      # N % 128
+    assert L.h3_gemm_fp8(p, p, p, p, 8, 256, 64, p, None) == 1       # K % 128
+    assert L.h3_gemm_fp8(p + 8, p, p, p, 8, 256, 256, p, None) == 1  # misaligned A
+    desc = lib.BlockDesc.make(L=64, d=256, n_heads=2)
+    assert lib.h3_workspace_size_fp8(desc) > lib.h3_workspace_size(desc)
+    assert lib.h3_mlp_workspace_size_fp8(lib.MlpDesc.make(L=64, d=256)) > 0
