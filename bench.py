@@ -51,6 +51,23 @@ def _peaks():
         return FALLBACK_PEAKS, "fallback"
 
 
+# ---------------------------------------------------------------------------- ranks
+def max_over_ranks(value: float, world: int, device) -> float:
+    """The largest per-rank value (the slowest replica sets the job's time)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(per_rank_work: float, world: int, max_ms: float) -> float:
+    """Whole-job rate: the work every replica did, over the slowest replica's time."""
+    return world * per_rank_work / (max_ms * 1e-3)
+
+
 # ---------------------------------------------------------------------------- clocks
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -256,10 +273,7 @@ def run_gpu(args, cfg):
     names = ["modulate", "qkv_rope_gemm", "attention", "out_gemm"]
     per = {n: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in evs)
            for i, n in enumerate(names)}
-    if world > 1:
-        tt = torch.tensor([ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(ms, world, dev)
 
     # ---- end to end through the public API with host buffers: every step uploads
     # its input x and modulation vectors from pinned host memory and downloads its
@@ -315,10 +329,7 @@ def run_gpu(args, cfg):
     e1.record(cs)
     torch.cuda.synchronize(dev)
     e2e_ms = e0.elapsed_time(e1) / args.steps
-    if world > 1:
-        tt = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
+    e2e_ms = max_over_ranks(e2e_ms, world, dev)
     st = h3.h3_sync_status(stream)
     if st != 0:
         raise RuntimeError(f"device status after e2e steps: {h3.h3_status_string(st)}")
@@ -458,7 +469,7 @@ def run_gpu(args, cfg):
     del zl, vl, x0l, flush
 
     flops = cfg.flops()
-    value = world * flops / (ms * 1e-3) / 1e12
+    value = job_throughput(flops, world, ms) / 1e12
     attn_flops = 4.0 * L * L * d
     peaks, peak_kind = _peaks()
     peak = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
@@ -484,14 +495,14 @@ def run_gpu(args, cfg):
                    "l2": f"inputs larger than L2 (x {L * d * 2 / 1e6:.0f} MB, qkv "
                          f"{L * 3 * d * 2 / 1e9:.2f} GB per step)",
                    "parallelism": f"replicas x{world}"},
-        "tokens_per_s": world * L / (ms * 1e-3),
+        "tokens_per_s": job_throughput(L, world, ms),
         "pct_of_bf16_peak_block": flops / (ms * 1e-3) / 1e12 / peak,
         "kernel_ms": per,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "kernel": "attention (attn_fwd_kernel)",
                      "peak_kind": f"{peak_kind} bf16 sustained (kernel inside a long step)"},
-        "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+        "e2e": {"value": job_throughput(flops, world, e2e_ms) / 1e12, "unit": UNIT,
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "sweep50": {"steps": 50, "total_ms": sweep_total,
                     "per_step_ms": {"median": statistics.median(sweep_steps),
