@@ -398,7 +398,8 @@ def run_gpu(args, cfg):
 
     # ---- the fp8 (E4M3) variants: both projections of the attention block and of
     # the MLP in fp8 (weights quantised per output channel once, activations per
-    # token on every call); attention itself stays bf16
+    # token on every call); the attention block's scores from E4M3 Q and K
+    # (per-token / per-key-block scales), P.V in bf16
     def quant(w):
         q = torch.empty(w.shape, dtype=torch.uint8, device=dev)
         sc8 = torch.empty(w.shape[0], dtype=torch.float32, device=dev)
@@ -426,7 +427,21 @@ def run_gpu(args, cfg):
         return ea.elapsed_time(eb) / n
 
     fp8_block_ms = timed(fp8_block)
-    del ws8, out8, wqkv8, wo8
+    # the fp8-score attention on its own (its Q/K quantisation included), on the
+    # rotated qkv the fp8 block left in its workspace
+    r256 = lambda n: (n + 255) // 256 * 256
+    qkv8 = ws8[r256(L * d * 2):r256(L * d * 2) + L * 3 * d * 2].view(torch.bfloat16).view(L, 3 * d)
+    a8bytes = h3.h3_attn_workspace_size_fp8(L, H)
+    aws8 = torch.empty(a8bytes, dtype=torch.uint8, device=dev)
+    o8 = torch.empty(L, d, dtype=torch.bfloat16, device=dev)
+    attn_fp8_ms = timed(lambda: h3.h3_joint_attn_fwd_fp8(qkv8, L, H, 128, 0, None, aws8, a8bytes,
+                                                         o8, stream=stream))
+    sq8 = aws8[r256(L * 2 * d):r256(L * 2 * d) + H * L * 4].view(torch.float32)
+    sk_off = r256(L * 2 * d) + r256(H * L * 4)
+    sk8 = aws8[sk_off:sk_off + H * ((L + 127) // 128) * 4].view(torch.float32)
+    quant_qk_ms = timed(lambda: h3.h3_quantize_qk_fp8(qkv8, L, H, 128, aws8, sq8, sk8,
+                                                      stream=stream))
+    del ws8, out8, wqkv8, wo8, aws8, o8
     g8 = torch.Generator(device="cpu").manual_seed(11)
     w1f = (torch.randn(4 * d, d, generator=g8) / d ** 0.5).to(torch.bfloat16).to(dev)
     w2f = (torch.randn(d, 4 * d, generator=g8) / (4 * d) ** 0.5).to(torch.bfloat16).to(dev)
@@ -519,10 +534,14 @@ def run_gpu(args, cfg):
                       "frac_of_sustained_bf16_peak": mlp_flops / (mlp_ms * 1e-3) / 1e12 / peak},
         "fp8": {"attn_block_ms": fp8_block_ms,
                 "attn_block_tflops": cfg.flops() / (fp8_block_ms * 1e-3) / 1e12,
+                "attention_ms": attn_fp8_ms,
+                "attention_tflops": 4.0 * L * L * d / (attn_fp8_ms * 1e-3) / 1e12,
+                "quantize_qk_ms": quant_qk_ms,
                 "mlp_block_ms": fp8_mlp_ms,
                 "mlp_block_tflops": mlp_flops / (fp8_mlp_ms * 1e-3) / 1e12,
-                "note": "projections in E4M3 (tcgen05 kind::f8f6f4), attention bf16; FLOPs "
-                        "counted as for the bf16 block"},
+                "note": "projections in E4M3 (tcgen05 kind::f8f6f4); attention scores from "
+                        "E4M3 Q and K, P.V in bf16; attention_ms includes the Q/K "
+                        "quantisation; FLOPs counted as for the bf16 block"},
         "denoise_step": {"L": L, "C": C_lat, "ms": denoise_ms,
                          "gbs": denoise_bytes / (denoise_ms * 1e-3) / 1e9,
                          "frac_of_hbm_peak": denoise_bytes / (denoise_ms * 1e-3) / 1e9

@@ -252,9 +252,40 @@ h3_status h3_gemm_fp8(const uint8_t* A, const float* a_scale, const uint8_t* B,
                       h3_stream_t stream);
 
 /*
+ * Joint attention with E4M3 scores ([vLLM] §6 Boundary Trimming for Packed
+ * Attention names quantised attention kernels as prior art; this is the form
+ * that quantises Q and K and keeps P V in bf16).  Same result as
+ * h3_joint_attn_fwd up to the E4M3 rounding of Q and K:
+ *   sq[h][i] = max_c |Q[i][h][c]| / 448          (one scale per token and head)
+ *   sk[h][b] = max over tokens 128b..128b+127 and c of |K[i][h][c]| / 448
+ *   Q8 = E4M3(Q / sq), K8 = E4M3(K / sk)          (round-to-nearest, saturating;
+ *                                                   scale 1 for all-zero data)
+ *   s_ij = sm_scale * sq[h][i] * sk[h][j/128] * (Q8_i . K8_j),  O = softmax(s) V
+ * with V, P and O in bf16 and fp32 accumulation as in h3_joint_attn_fwd.
+ *   qkv [L][3 * n_heads * 128] bf16 (Q, K after the rotary embedding) ->
+ *   O [L][n_heads * 128] bf16, lse [n_heads][L] fp32 or NULL; causal 0 or 1.
+ *   workspace: >= h3_attn_workspace_size_fp8(L, n_heads, 128) bytes, 256-byte
+ *   aligned, caller-owned, holding qk8 [L][2 * n_heads * 128] bytes (Q8 | K8),
+ *   then sq [n_heads][L] and sk [n_heads][ceil(L / 128)] fp32, each region at a
+ *   256-byte boundary.  No cu_seqlens form.
+ * h3_quantize_qk_fp8 is the first of the two launches on its own: it writes
+ * qk8, sq and sk as above (qk8 8-byte aligned; sq, sk 4-byte aligned).
+ */
+h3_status h3_attn_workspace_size_fp8(int32_t L, int32_t n_heads, int32_t head_dim,
+                                     size_t* bytes);
+h3_status h3_quantize_qk_fp8(const uint16_t* qkv, int32_t L, int32_t n_heads, int32_t head_dim,
+                             uint8_t* qk8, float* sq, float* sk, h3_stream_t stream);
+h3_status h3_joint_attn_fwd_fp8(const uint16_t* qkv, int32_t L, int32_t n_heads,
+                                int32_t head_dim, int32_t causal, float sm_scale,
+                                void* workspace, size_t workspace_bytes, uint16_t* O, float* lse,
+                                h3_stream_t stream);
+
+/*
  * h3_attn_block_fwd with the two projections in FP8: y and O are quantised
  * per token before the QKV projection (RoPE in its epilogue) and the output
- * projection (gated residual in its epilogue); attention stays bf16.
+ * projection (gated residual in its epilogue).  Without segments
+ * (desc->n_seg == 0) the attention takes E4M3 scores as in
+ * h3_joint_attn_fwd_fp8; with segments it stays bf16.
  *   Wqkv_q [3d][d], Wo_q [d][d]: E4M3 weights from h3_quantize_rows_fp8, with
  *   their per-output-channel scales Wqkv_s [3d], Wo_s [d].
  * workspace >= h3_workspace_size_fp8(desc) bytes, 256-byte aligned.

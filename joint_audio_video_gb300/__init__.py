@@ -25,6 +25,7 @@ __all__ = [
     "h3_denoise_step", "MlpDesc", "h3_mlp_workspace_size", "h3_mlp_block_fwd",
     "h3_quantize_rows_fp8", "h3_gemm_fp8", "h3_workspace_size_fp8", "h3_attn_block_fwd_fp8",
     "h3_mlp_workspace_size_fp8", "h3_mlp_block_fwd_fp8",
+    "h3_attn_workspace_size_fp8", "h3_quantize_qk_fp8", "h3_joint_attn_fwd_fp8",
     "NOALLOC_SCRATCH_BYTES", "EXPORTED_SYMBOLS",
 ]
 
@@ -44,6 +45,7 @@ EXPORTED_SYMBOLS = (
     "h3_denoise_step", "h3_mlp_workspace_size", "h3_mlp_block_fwd",
     "h3_quantize_rows_fp8", "h3_gemm_fp8", "h3_workspace_size_fp8", "h3_attn_block_fwd_fp8",
     "h3_mlp_workspace_size_fp8", "h3_mlp_block_fwd_fp8",
+    "h3_attn_workspace_size_fp8", "h3_quantize_qk_fp8", "h3_joint_attn_fwd_fp8",
 )
 
 # Workspace the library keeps per GPU for h3_attn_block_fwd_noalloc.
@@ -127,6 +129,10 @@ def _sig(lib):
                                               ctypes.POINTER(ctypes.c_size_t)]
     lib.h3_mlp_block_fwd_fp8.argtypes = ([ctypes.POINTER(MlpDesc)] + [_P] * 10 +
                                          [ctypes.c_size_t, _P, _P])
+    lib.h3_attn_workspace_size_fp8.argtypes = [_I, _I, _I, ctypes.POINTER(ctypes.c_size_t)]
+    lib.h3_quantize_qk_fp8.argtypes = [_P, _I, _I, _I, _P, _P, _P, _P]
+    lib.h3_joint_attn_fwd_fp8.argtypes = [_P, _I, _I, _I, _I, ctypes.c_float, _P,
+                                          ctypes.c_size_t, _P, _P, _P]
     lib.h3_sync_status.argtypes = [_P]
     lib.h3_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
     lib.h3_set_wait_limit_ns.restype = None
@@ -318,6 +324,27 @@ def h3_quantize_rows_fp8(x, R, K, q, scale, stream=None) -> None:
 def h3_gemm_fp8(A, a_scale, B, b_scale, M, N, K, C, stream=None) -> None:
     _check("h3_gemm_fp8", load().h3_gemm_fp8(_addr(A), _addr(a_scale), _addr(B), _addr(b_scale),
                                              M, N, K, _addr(C), _stream(stream)))
+
+
+def h3_attn_workspace_size_fp8(L, n_heads, head_dim=128) -> int:
+    n = ctypes.c_size_t(0)
+    _check("h3_attn_workspace_size_fp8",
+           load().h3_attn_workspace_size_fp8(L, n_heads, head_dim, ctypes.byref(n)))
+    return int(n.value)
+
+
+def h3_quantize_qk_fp8(qkv, L, n_heads, head_dim, qk8, sq, sk, stream=None) -> None:
+    _check("h3_quantize_qk_fp8", load().h3_quantize_qk_fp8(
+        _addr(qkv), L, n_heads, head_dim, _addr(qk8), _addr(sq), _addr(sk), _stream(stream)))
+
+
+def h3_joint_attn_fwd_fp8(qkv, L, n_heads, head_dim, causal, sm_scale, workspace,
+                          workspace_bytes, O, lse=None, stream=None) -> None:
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(head_dim)
+    _check("h3_joint_attn_fwd_fp8", load().h3_joint_attn_fwd_fp8(
+        _addr(qkv), L, n_heads, head_dim, int(bool(causal)), sm_scale, _addr(workspace),
+        int(workspace_bytes), _addr(O), _addr(lse), _stream(stream)))
 
 
 def h3_workspace_size_fp8(desc: BlockDesc) -> int:

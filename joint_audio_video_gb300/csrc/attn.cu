@@ -24,6 +24,13 @@
 // Softmax works in the log2 domain with a per-row running maximum that is
 // only moved (and O, l rescaled in TMEM) when the block maximum exceeds it by
 // more than 8 (factor 256): the final O / l is exact for any such maximum.
+//
+// FP8 scores (the quantised-attention prior art that §6 of "Joint Audio-Video
+// Generation in Production" names, in the form that keeps P.V in bf16): Q and
+// K arrive as E4M3 (128 bytes per head row, one 16 KB box per tile) with a
+// per-token Q scale and a per-128-key-block K scale; S = Q8 K8^T runs as four
+// kind::f8f6f4 products of K = 32, and the two scales fold into the softmax's
+// per-row, per-block constant: s = sq[i] sk[b] (q8 . k8).
 #include <cuda_bf16.h>
 
 #include "kernels.hpp"
@@ -37,6 +44,7 @@ constexpr int kThreads = 320;
 constexpr int kStages = 4;
 constexpr uint32_t kTile = 128 * 128 * 2;     // one 128x128 bf16 tile (two 16 KB boxes)
 constexpr uint32_t kBox = 128 * 64 * 2;
+constexpr uint32_t kTile8 = 128 * 128;        // one 128x128 E4M3 tile (one 16 KB box)
 constexpr size_t kSmem = 2 * kTile + kStages * kTile + 1024;
 constexpr float kRescaleThreshold = 8.0f;     // log2 units
 
@@ -51,6 +59,9 @@ struct AttnDev {
   uint64_t wait_ns;
   int n_seg;                      // 0: one segment [0, L)
   int32_t cu[kMaxSegments + 1];   // segment starts, cu[n_seg] = L
+  const float* sq;                // fp8 scores: [H][L] Q scales
+  const float* sk;                // fp8 scores: [H][nkb] K block scales
+  int nkb;
 };
 
 // Segment of token i: the last s with cu[s] <= i (skips empty segments).
@@ -143,12 +154,21 @@ __device__ __forceinline__ void exp32(const uint32_t (&r)[32], uint64_t cc, uint
 // 128x128x16 MMA (64 tensor-core cycles) must cost far less than 64 cycles
 // of the issuing thread, or the tensor core waits on the issuer.
 // S = Q K^T: both K-major, 8 steps of K=16 over the two 64-column boxes.
+template <bool FP8>
 __device__ __forceinline__ void s_product(uint32_t d_tmem, SDesc q, SDesc k) {
-  constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 0, 0);
+  if constexpr (FP8) {
+    // E4M3: one 128-byte row holds the head's 128 dims; 4 steps of K = 32
+    constexpr uint32_t idesc = idesc_e4m3_f32(128, 128);
 #pragma unroll
-  for (int s = 0; s < 8; ++s) {
-    const uint32_t off = (s >> 2) * kBox + (s & 3) * 32;
-    mma_bf16_ss(d_tmem, sdesc_at(q, off), sdesc_at(k, off), idesc, s > 0);
+    for (int s = 0; s < 4; ++s)
+      mma_f8_ss(d_tmem, sdesc_at(q, s * 32), sdesc_at(k, s * 32), idesc, s > 0);
+  } else {
+    constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 0, 0);
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+      const uint32_t off = (s >> 2) * kBox + (s & 3) * 32;
+      mma_bf16_ss(d_tmem, sdesc_at(q, off), sdesc_at(k, off), idesc, s > 0);
+    }
   }
 }
 
@@ -164,8 +184,10 @@ __device__ __forceinline__ void pv_product(uint32_t o_tmem, uint32_t p_tmem, SDe
 // Registers are split over the SM's four sub-partitions (16K each) and warp w
 // runs on sub-partition w % 4, so with 10 warps three share one sub-partition:
 // at most 168 registers per thread.
+template <bool FP8>
 __global__ void __launch_bounds__(kThreads, 1)
-    attn_fwd_kernel(const __grid_constant__ CUtensorMap tm, const __grid_constant__ AttnDev p) {
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tm, const __grid_constant__ CUtensorMap tm8,
+                    const __grid_constant__ AttnDev p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t bar_q, bar_kv_full[kStages], bar_kv_empty[kStages], bar_s[2], bar_p[2],
       bar_o, bar_drain;
@@ -211,7 +233,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(smem_u32(&tmem_base_sh), 512);
     tmem_relinquish();
   }
-  if (warp == 0 && lane_id() == 0) tma_prefetch_desc(&tm);
+  if (warp == 0 && lane_id() == 0) {
+    tma_prefetch_desc(&tm);
+    if (FP8) tma_prefetch_desc(&tm8);
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -222,11 +247,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane_id() == 0) {
       const int xq = h * 128, xk = p.d + h * 128, xv = 2 * p.d + h * 128;
       const uint32_t qb = smem_u32(&bar_q);
-      mbar_arrive_expect_tx(qb, 2 * kTile);
-      tma_load_2d(sQ, &tm, qb, xq, q0);
-      tma_load_2d(sQ + kBox, &tm, qb, xq + 64, q0);
-      tma_load_2d(sQ + kTile, &tm, qb, xq, q0 + 128);
-      tma_load_2d(sQ + kTile + kBox, &tm, qb, xq + 64, q0 + 128);
+      if (FP8) {   // E4M3 Q | K rows: Q at byte column h*128, K at d + h*128
+        mbar_arrive_expect_tx(qb, 2 * kTile8);
+        tma_load_2d(sQ, &tm8, qb, xq, q0);
+        tma_load_2d(sQ + kTile, &tm8, qb, xq, q0 + 128);
+      } else {
+        mbar_arrive_expect_tx(qb, 2 * kTile);
+        tma_load_2d(sQ, &tm, qb, xq, q0);
+        tma_load_2d(sQ + kBox, &tm, qb, xq + 64, q0);
+        tma_load_2d(sQ + kTile, &tm, qb, xq, q0 + 128);
+        tma_load_2d(sQ + kTile + kBox, &tm, qb, xq + 64, q0 + 128);
+      }
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
@@ -236,9 +267,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t fb = smem_u32(&bar_kv_full[stage]);
           const uint32_t dst = sRing + stage * kTile;
           const int x = kv == 0 ? xk : xv;
-          mbar_arrive_expect_tx(fb, kTile);
-          tma_load_2d(dst, &tm, fb, x, kv_lo + j * 128);
-          tma_load_2d(dst + kBox, &tm, fb, x + 64, kv_lo + j * 128);
+          if (FP8 && kv == 0) {
+            mbar_arrive_expect_tx(fb, kTile8);
+            tma_load_2d(dst, &tm8, fb, x, kv_lo + j * 128);
+          } else {
+            mbar_arrive_expect_tx(fb, kTile);
+            tma_load_2d(dst, &tm, fb, x, kv_lo + j * 128);
+            tma_load_2d(dst + kBox, &tm, fb, x + 64, kv_lo + j * 128);
+          }
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
       }
@@ -280,9 +316,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (ok) {
         tc_fence_after();
-        s_product(tS0, dQ0, dK(kA));
+        s_product<FP8>(tS0, dQ0, dK(kA));
         tc_commit(smem_u32(&bar_s[0]));
-        s_product(tS1, dQ1, dK(kA));
+        s_product<FP8>(tS1, dQ1, dK(kA));
         tc_commit(smem_u32(&bar_s[1]));
         tc_commit(kv_empty(0));
       }
@@ -295,14 +331,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         tc_fence_after();
         pv_product(tO0, tS0, dV(vA), j > 1);
-        s_product(tS0, dQ0, dK(kA));
+        s_product<FP8>(tS0, dQ0, dK(kA));
         tc_commit(smem_u32(&bar_s[0]));
         ok = mbar_wait(smem_u32(&bar_p[1]), pph, wc);
         if (!ok) break;
         tc_fence_after();
         pv_product(tO1, tS1, dV(vA), j > 1);
         tc_commit(kv_empty(2 * j - 1));
-        s_product(tS1, dQ1, dK(kA));
+        s_product<FP8>(tS1, dQ1, dK(kA));
         tc_commit(smem_u32(&bar_s[1]));
         tc_commit(kv_empty(2 * j));
       }
@@ -349,8 +385,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (p.causal) row_hi = min(row_hi, qi + 1);
     float m_used = -INFINITY, l = 0.f;
+    // exponent constant: sm_scale log2(e), times the row's Q scale for fp8 scores
+    float c_row = p.scale_log2;
+    if (FP8) c_row *= p.sq[size_t(h) * p.L + min(qi, p.L - 1)];
     bool ok = true;
     for (int j = 0; j < nblk; ++j) {
+      // ... and the key block's K scale (fp8 scores have kv_lo = 0)
+      const float c = FP8 ? c_row * p.sk[size_t(h) * p.nkb + j] : c_row;
       ok = __all_sync(0xffffffffu, mbar_wait(bs, j & 1, wc));
       if (!ok) break;
       tc_fence_after();
@@ -378,7 +419,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // row maximum of the raw scores (scale > 0 commutes with max); -inf while
       // no key of this row has been seen, and then O and l hold only zeros
-      const float mx = max128(r0, r1, r2, r3) * p.scale_log2;
+      const float mx = max128(r0, r1, r2, r3) * c;
       {
         const float m_new = fmaxf(m_used, mx);
         const bool fresh = m_used == -INFINITY;
@@ -402,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // p = 2^(s * scale_log2 - m_used), rounded to bf16 pairs over S's first 64 columns
       const float neg_m = m_used == -INFINITY ? 0.f : -m_used;   // all scores -inf: p = 0
-      const uint64_t cc = f2(p.scale_log2, p.scale_log2), nm = f2(neg_m, neg_m);
+      const uint64_t cc = f2(c, c), nm = f2(neg_m, neg_m);
       uint64_t acc[2] = {0ull, 0ull};
       uint32_t pk0[32], pk1[32];
       exp32(r0, cc, nm, pk0, acc);
@@ -456,8 +497,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 cudaError_t launch_attention(const AttnArgs& a, const DevCtx& ctx, cudaStream_t st) {
   const int d = a.H * 128;
-  CUtensorMap tm;
+  CUtensorMap tm, tm8;
   if (!make_tmap_bf16_2d(&tm, a.qkv, a.L, 3 * d, 3 * d, 128, 64)) return cudaErrorInvalidValue;
+  if (a.fp8) {
+    if (a.n_seg != 0 || a.qk8 == nullptr || a.sq == nullptr || a.sk == nullptr)
+      return cudaErrorInvalidValue;
+    if (!make_tmap_u8_2d(&tm8, a.qk8, a.L, 2 * d, 2 * d, 128)) return cudaErrorInvalidValue;
+  } else {
+    tm8 = tm;   // unused
+  }
   AttnDev p{};
   p.O = static_cast<__nv_bfloat16*>(a.O);
   p.lse = a.lse;
@@ -471,11 +519,14 @@ cudaError_t launch_attention(const AttnArgs& a, const DevCtx& ctx, cudaStream_t 
   p.wait_ns = ctx.wait_ns;
   p.n_seg = a.n_seg;
   for (int i = 0; i <= a.n_seg && a.cu_seqlens; ++i) p.cu[i] = a.cu_seqlens[i];
-  cudaError_t e =
-      cudaFuncSetAttribute(attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmem));
+  p.sq = a.sq;
+  p.sk = a.sk;
+  p.nkb = (a.L + 127) / 128;
+  auto kernel = a.fp8 ? attn_fwd_kernel<true> : attn_fwd_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmem));
   if (e != cudaSuccess) return e;
   const long long grid = (long long)p.num_pairs * a.H;
-  attn_fwd_kernel<<<unsigned(grid), kThreads, kSmem, st>>>(tm, p);
+  kernel<<<unsigned(grid), kThreads, kSmem, st>>>(tm, tm8, p);
   return cudaGetLastError();
 }
 

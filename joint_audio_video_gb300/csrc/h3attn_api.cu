@@ -236,6 +236,85 @@ h3_status h3_joint_attn_varlen_fwd(const uint16_t* qkv, const int32_t* cu_seqlen
   return launched(launch_attention(a, ctx, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+// Workspace of the fp8-score attention: qk8 [L][2d] bytes | sq [H][L] | sk [H][nkb].
+static size_t attn_fp8_bytes(size_t L, size_t H) {
+  const size_t d = H * 128, nkb = (L + 127) / 128;
+  return round256(L * 2 * d) + round256(H * L * 4) + round256(H * nkb * 4);
+}
+
+h3_status h3_attn_workspace_size_fp8(int32_t L, int32_t n_heads, int32_t head_dim,
+                                     size_t* bytes) {
+  if (bytes == nullptr || L < 1 || n_heads < 1) return H3_ERR_INVALID_ARG;
+  if (head_dim != 128) return H3_ERR_UNSUPPORTED;
+  if (!valid_d(n_heads * 128)) return H3_ERR_INVALID_ARG;
+  *bytes = attn_fp8_bytes(size_t(L), size_t(n_heads));
+  return H3_OK;
+}
+
+h3_status h3_quantize_qk_fp8(const uint16_t* qkv, int32_t L, int32_t n_heads, int32_t head_dim,
+                             uint8_t* qk8, float* sq, float* sk, h3_stream_t stream) {
+  if (L < 1 || n_heads < 1) return H3_ERR_INVALID_ARG;
+  if (head_dim != 128) return H3_ERR_UNSUPPORTED;
+  if (!valid_d(n_heads * 128)) return H3_ERR_INVALID_ARG;
+  if (!aligned16(qkv) || !aligned16(qk8) || sq == nullptr || sk == nullptr ||
+      (reinterpret_cast<uintptr_t>(sq) & 3u) || (reinterpret_cast<uintptr_t>(sk) & 3u))
+    return H3_ERR_INVALID_ARG;
+  const size_t d = size_t(n_heads) * 128, nkb = (size_t(L) + 127) / 128;
+  const size_t qkv_b = size_t(L) * 3 * d * 2;
+  if (overlap(qkv, qkv_b, qk8, size_t(L) * 2 * d) ||
+      overlap(qkv, qkv_b, sq, size_t(n_heads) * L * 4) ||
+      overlap(qkv, qkv_b, sk, size_t(n_heads) * nkb * 4))
+    return H3_ERR_INVALID_ARG;
+  DevCtx ctx;
+  if (h3_status s = dev_ctx(&ctx)) return s;
+  return launched(launch_quantize_qk(qkv, L, n_heads, qk8, sq, sk, ctx,
+                                     reinterpret_cast<cudaStream_t>(stream)));
+}
+
+h3_status h3_joint_attn_fwd_fp8(const uint16_t* qkv, int32_t L, int32_t n_heads,
+                                int32_t head_dim, int32_t causal, float sm_scale,
+                                void* workspace, size_t workspace_bytes, uint16_t* O, float* lse,
+                                h3_stream_t stream) {
+  if (L < 1 || n_heads < 1) return H3_ERR_INVALID_ARG;
+  if (head_dim != 128) return H3_ERR_UNSUPPORTED;
+  if (!valid_d(n_heads * 128)) return H3_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return H3_ERR_INVALID_ARG;
+  if (!(sm_scale > 0.f) || !std::isfinite(sm_scale)) return H3_ERR_INVALID_ARG;
+  if (!aligned16(qkv) || !aligned16(O) || workspace == nullptr ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return H3_ERR_INVALID_ARG;
+  if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u)) return H3_ERR_INVALID_ARG;
+  const size_t need = attn_fp8_bytes(size_t(L), size_t(n_heads));
+  if (workspace_bytes < need) return H3_ERR_WORKSPACE;
+  const size_t d = size_t(n_heads) * 128;
+  const size_t qkv_b = size_t(L) * 3 * d * 2, o_b = size_t(L) * d * 2;
+  if (overlap(qkv, qkv_b, O, o_b) || overlap(workspace, need, qkv, qkv_b) ||
+      overlap(workspace, need, O, o_b) ||
+      (lse != nullptr && overlap(workspace, need, lse, size_t(n_heads) * L * 4)))
+    return H3_ERR_INVALID_ARG;
+  DevCtx ctx;
+  if (h3_status s = dev_ctx(&ctx)) return s;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint8_t* qk8 = ws;
+  float* sq = reinterpret_cast<float*>(ws + round256(size_t(L) * 2 * d));
+  float* sk = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(sq) + round256(size_t(n_heads) * L * 4));
+  if (launch_quantize_qk(qkv, L, n_heads, qk8, sq, sk, ctx, st) != cudaSuccess) return H3_ERR_CUDA;
+  AttnArgs a{};
+  a.qkv = qkv;
+  a.O = O;
+  a.lse = lse;
+  a.L = L;
+  a.H = n_heads;
+  a.causal = causal;
+  a.sm_scale = sm_scale;
+  a.fp8 = 1;
+  a.qk8 = qk8;
+  a.sq = sq;
+  a.sk = sk;
+  return launched(launch_attention(a, ctx, st));
+}
+
 h3_status h3_out_proj_gated_residual(const uint16_t* O, const uint16_t* Wo,
                                      const uint16_t* x_res, const uint8_t* mod,
                                      const float* gate, int32_t L, int32_t d, int32_t n_mod,
@@ -398,6 +477,7 @@ h3_status h3_workspace_size_fp8(const h3_block_desc* desc, size_t* bytes) {
   if (h3_status s = check_desc(desc)) return s;
   const size_t L = size_t(desc->L), d = size_t(desc->d);
   *bytes = round256(L * d * 2) + round256(L * 3 * d * 2) + round256(L * d) + round256(L * 4);
+  if (desc->n_seg == 0) *bytes += attn_fp8_bytes(L, size_t(desc->n_heads));
   return H3_OK;
 }
 
@@ -457,6 +537,18 @@ h3_status h3_attn_block_fwd_fp8(const h3_block_desc* desc, const uint16_t* x, co
   a.sm_scale = 1.0f / std::sqrt(float(desc->head_dim));
   a.n_seg = desc->n_seg;
   a.cu_seqlens = desc->cu_seqlens;
+  if (desc->n_seg == 0) {   // E4M3 scores; per-segment attention stays bf16
+    uint8_t* qk8 = static_cast<uint8_t*>(q8) + round256(L * d) + round256(L * 4);
+    float* sq = reinterpret_cast<float*>(qk8 + round256(L * 2 * d));
+    float* sk = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(sq) +
+                                         round256(size_t(desc->n_heads) * L * 4));
+    if (launch_quantize_qk(qkv, Li, desc->n_heads, qk8, sq, sk, ctx, st) != cudaSuccess)
+      return H3_ERR_CUDA;
+    a.fp8 = 1;
+    a.qk8 = qk8;
+    a.sq = sq;
+    a.sk = sk;
+  }
   if (launch_attention(a, ctx, st) != cudaSuccess ||
       launch_quantize_rows(y, Li, di, q8, s8, ctx, st) != cudaSuccess)
     return H3_ERR_CUDA;

@@ -66,11 +66,21 @@ struct AttnArgs {
   float sm_scale;
   int n_seg;                  // 0: one segment [0, L)
   const int32_t* cu_seqlens;  // host array [n_seg + 1], validated, n_seg <= kMaxSegments
+  // E4M3 scores (n_seg == 0 only): Q and K from qk8 [L][2*H*128] bytes (Q | K),
+  // sq [H][L] per-token Q scales, sk [H][ceil(L/128)] per-key-block K scales;
+  // V is still read as bf16 from qkv.
+  int fp8 = 0;
+  const void* qk8 = nullptr;
+  const float* sq = nullptr;
+  const float* sk = nullptr;
 };
 
 cudaError_t launch_attention(const AttnArgs& a, const DevCtx& ctx, cudaStream_t st);
 
 // Row-wise E4M3 quantisation: q[r] = RN(x[r] / s[r]) with s[r] = max|x[r]| / 448.
+// E4M3 Q and K for the fp8 scores: per-token Q scale, per-128-key-block K scale.
+cudaError_t launch_quantize_qk(const void* qkv, int L, int H, void* qk8, float* sq, float* sk,
+                               const DevCtx& ctx, cudaStream_t st);
 cudaError_t launch_quantize_rows(const void* x, int R, int K, void* q, float* scale,
                                  const DevCtx& ctx, cudaStream_t st);
 

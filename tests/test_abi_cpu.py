@@ -30,7 +30,7 @@ def _declared():
 
 def test_library_exports_every_declared_entry_point(lib):
     names = _declared()
-    assert len(names) == 25, names
+    assert len(names) == 28, names
     raw = ctypes.CDLL(lib.lib_path)
     for n in names:
         assert hasattr(raw, n), f"{n} declared but not exported"
@@ -190,3 +190,43 @@ def test_fp8_arguments_are_validated_before_launch(lib):
     desc = lib.BlockDesc.make(L=64, d=256, n_heads=2)
     assert lib.h3_workspace_size_fp8(desc) > lib.h3_workspace_size(desc)
     assert lib.h3_mlp_workspace_size_fp8(lib.MlpDesc.make(L=64, d=256)) > 0
+
+
+def test_fp8_attention_arguments_are_validated_before_launch(lib):
+    L = lib.load()
+    p = 1 << 20
+    r = lambda x: (x + 255) // 256 * 256
+    # workspace: qk8 [L][2d] bytes | sq [H][L] fp32 | sk [H][ceil(L/128)] fp32
+    for Lt, H in ((1, 1), (300, 2), (58758, 40)):
+        assert lib.h3_attn_workspace_size_fp8(Lt, H) == (
+            r(Lt * 2 * H * 128) + r(H * Lt * 4) + r(H * ((Lt + 127) // 128) * 4))
+    n = ctypes.c_size_t(0)
+    assert L.h3_attn_workspace_size_fp8(0, 2, 128, ctypes.byref(n)) == 1
+    assert L.h3_attn_workspace_size_fp8(64, 2, 64, ctypes.byref(n)) == 2
+    assert L.h3_attn_workspace_size_fp8(64, 2, 128, None) == 1
+    big = 1 << 28
+    # quantiser: alignment, null scales, head size, overlap with its input
+    assert L.h3_quantize_qk_fp8(p + 8, 64, 2, 128, p + big, p + 2 * big, p + 3 * big, None) == 1
+    assert L.h3_quantize_qk_fp8(p, 64, 2, 128, p + big, None, p + 3 * big, None) == 1
+    assert L.h3_quantize_qk_fp8(p, 64, 2, 64, p + big, p + 2 * big, p + 3 * big, None) == 2
+    assert L.h3_quantize_qk_fp8(p, 64, 2, 128, p + 4096, p + 2 * big, p + 3 * big, None) == 1
+    assert L.h3_quantize_qk_fp8(p, 0, 2, 128, p + big, p + 2 * big, p + 3 * big, None) == 1
+    # attention: workspace size and alignment, causal flag, scale, overlaps
+    ws = lib.h3_attn_workspace_size_fp8(64, 2)
+    args = lambda **k: (k.get("qkv", p), 64, 2, 128, k.get("causal", 0), k.get("scale", 0.0884),
+                        k.get("ws", p + big), k.get("ws_bytes", ws), k.get("O", p + 2 * big),
+                        k.get("lse", None), None)
+    assert L.h3_joint_attn_fwd_fp8(*args(ws_bytes=ws - 1)) == 6
+    assert L.h3_joint_attn_fwd_fp8(*args(ws=p + big + 16)) == 1
+    assert L.h3_joint_attn_fwd_fp8(*args(causal=2)) == 1
+    assert L.h3_joint_attn_fwd_fp8(*args(scale=0.0)) == 1
+    assert L.h3_joint_attn_fwd_fp8(*args(scale=float("inf"))) == 1
+    assert L.h3_joint_attn_fwd_fp8(*args(O=p + big + 256)) == 1      # O inside the workspace
+    assert L.h3_joint_attn_fwd_fp8(*args(ws=p + 256)) == 1           # workspace over qkv
+    assert L.h3_joint_attn_fwd_fp8(*args(lse=p + big + 4)) == 1      # lse inside the workspace
+    assert L.h3_joint_attn_fwd_fp8(*args(O=p + 8)) == 1              # misaligned O
+    # the fused fp8 block needs the score workspace only without segments
+    d0 = lib.BlockDesc.make(L=64, d=256, n_heads=2)
+    d1 = lib.BlockDesc.make(L=64, d=256, n_heads=2, cu_seqlens=[0, 20, 64])
+    assert lib.h3_workspace_size_fp8(d0) - lib.h3_workspace_size_fp8(d1) == \
+        lib.h3_attn_workspace_size_fp8(64, 2)

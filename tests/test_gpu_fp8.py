@@ -11,21 +11,12 @@ import torch
 
 import oracle as orc
 from h3inputs import CONFIGS, block_inputs
+from tests._fp8 import e4m3_decode
 from tests._parity import assert_parity, to64
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
 FP8_MAX, FP8_MEAN = 16 * 2e-2, 16 * 5e-3
-
-
-def e4m3_decode(b: np.ndarray) -> np.ndarray:
-    """Value of E4M3 bytes (1 sign, 4 exponent bits with bias 7, 3 mantissa bits)."""
-    b = b.astype(np.int64)
-    sign = np.where(b & 0x80, -1.0, 1.0)
-    e = (b >> 3) & 0xF
-    m = b & 0x7
-    val = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1 + m / 8.0) * 2.0 ** (e - 7))
-    return sign * val
 
 
 def _quant(h3, x):
