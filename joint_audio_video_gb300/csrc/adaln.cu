@@ -5,8 +5,11 @@
 //   Joint Audio-Video Generation Complicates RL Training": modality-specific
 //   AdaLN branches whose outputs are cached per modality).
 //
-// One 256-thread CTA per token row.  The row (d bf16 = d/8 16-byte vectors)
-// is loaded once with streaming 16-byte loads and kept in registers; mean and
+// One 128-thread CTA per token row.  The row (d bf16 = d/8 16-byte vectors)
+// is loaded once with streaming 16-byte loads and kept in registers (5 vectors
+// per thread at d = 5120; at most 64 registers, so 8 rows, 80 KB, are in flight
+// per SM where 256-thread rows managed ~5: the bytes in flight set the HBM
+// rate this kernel reaches); mean and
 // variance are two exact passes over the registers (fp32 warp shuffles + a
 // shared-memory hop across the 8 warps).  The per-modality fp32 vectors are
 // tiny (n_mod x d) and served from L1/L2.  Algorithmic traffic: 4*d bytes per
@@ -19,7 +22,7 @@
 namespace h3 {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 128;
 
 __device__ __forceinline__ float block_sum(float v, float* red) {
 #pragma unroll
@@ -45,7 +48,7 @@ __device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
 }
 
 template <int VPT>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, VPT <= 5 ? 8 : 2)
     adaln_modulate_kernel(const uint4* __restrict__ x, const uint8_t* __restrict__ mod,
                           const float* __restrict__ shift, const float* __restrict__ scale, int d,
                           int n_mod, float eps, uint4* __restrict__ y, int* status) {
@@ -138,13 +141,18 @@ cudaError_t launch_adaln_modulate(const void* x, const uint8_t* mod, const float
                                   const float* scale, int L, int d, int n_mod, float eps, void* y,
                                   const DevCtx& ctx, cudaStream_t st) {
   const int vpt = (d / 8 + kThreads - 1) / kThreads;
-  switch (vpt) {
+  switch (vpt) {   // d <= 16384: at most 16 vectors per thread
     case 1: return launch_vpt<1>(x, mod, shift, scale, L, d, n_mod, eps, y, ctx, st);
     case 2: return launch_vpt<2>(x, mod, shift, scale, L, d, n_mod, eps, y, ctx, st);
     case 3: return launch_vpt<3>(x, mod, shift, scale, L, d, n_mod, eps, y, ctx, st);
     case 4: return launch_vpt<4>(x, mod, shift, scale, L, d, n_mod, eps, y, ctx, st);
-    case 5: case 6: return launch_vpt<6>(x, mod, shift, scale, L, d, n_mod, eps, y, ctx, st);
+    case 5: return launch_vpt<5>(x, mod, shift, scale, L, d, n_mod, eps, y, ctx, st);
+    case 6: return launch_vpt<6>(x, mod, shift, scale, L, d, n_mod, eps, y, ctx, st);
     case 7: case 8: return launch_vpt<8>(x, mod, shift, scale, L, d, n_mod, eps, y, ctx, st);
+    case 9: case 10: case 11: case 12:
+      return launch_vpt<12>(x, mod, shift, scale, L, d, n_mod, eps, y, ctx, st);
+    case 13: case 14: case 15: case 16:
+      return launch_vpt<16>(x, mod, shift, scale, L, d, n_mod, eps, y, ctx, st);
     default: return cudaErrorInvalidValue;
   }
 }
