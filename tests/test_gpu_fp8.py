@@ -120,3 +120,29 @@ def test_mlp_fp8_against_oracle(h3):
     r = orc.mlp_block(to64(x), mod, to64(sh), to64(sc), to64(gt), to64(w1), to64(w2))
     assert_parity(to64(out), r["out"], "small fp8 mlp out", max_rel_rms=FP8_MAX,
                   mean_rel=FP8_MEAN, bf16_storage=False)
+
+
+def test_block_fp8_with_segments_against_oracle(h3):
+    """With cu_seqlens the fp8 block keeps its fp8 projections and attends per
+    segment in bf16 (the fp8 scores are for the unsegmented sequence only)."""
+    c = CONFIGS["small"]
+    cu = [0, c.n_text, c.n_text + c.n_video, c.L]
+    inp = block_inputs(c)
+    args = (c.n_text, c.video_t, c.video_h, c.video_w, c.audio_channels, c.audio_steps)
+    mod, pos = h3.h3_build_packed_layout(*args)
+    omod, opos = orc.packed_layout(*args)
+    desc = h3.BlockDesc.make(L=c.L, d=c.d, n_heads=c.n_heads, cu_seqlens=cu)
+    nbytes = h3.h3_workspace_size_fp8(desc)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=DEV)
+    out = torch.full((c.L, c.d), float("nan"), dtype=torch.bfloat16, device=DEV)
+    dv = {k: v.to(DEV) for k, v in inp.items() if k != "x_raw"}
+    wq, wqs, woq, wos = _quantized_weights(h3, inp["Wqkv"], inp["Wo"])
+    h3.h3_attn_block_fwd_fp8(desc, dv["x"], torch.from_numpy(mod).to(DEV),
+                             torch.from_numpy(pos).to(DEV), dv["shift"], dv["scale"], dv["gate"],
+                             wq, wqs, woq, wos, ws, nbytes, out)
+    assert h3.h3_sync_status() == 0
+    f = lambda k: to64(inp[k])
+    r = orc.block(f("x"), omod, opos, f("shift"), f("scale"), f("gate"), f("Wqkv"), f("Wo"),
+                  c.n_heads, cu_seqlens=cu)
+    assert_parity(to64(out), r["out"], "small fp8 block with segments", max_rel_rms=FP8_MAX,
+                  mean_rel=FP8_MEAN, bf16_storage=False)
