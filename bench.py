@@ -563,6 +563,101 @@ def run_gpu(args, cfg):
     return 0
 
 
+def run_library_context(args, cfg):
+    """Context, not the contract line: this library's block (full and causal)
+    next to PyTorch's fused attention (its cuDNN / flash / memory-efficient
+    backends, whichever run) and cuBLAS on the same shapes and the same rotated
+    Q, K, V, one GPU, CUDA events, 3 warm-up and `steps` timed calls each."""
+    import torch
+    import torch.nn.functional as F
+    import joint_audio_video_gb300 as h3
+    from joint_audio_video_gb300 import build as h3build
+    from h3inputs import block_inputs
+
+    h3build.build()
+    h3.load()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    L, d, H = cfg.L, cfg.d, cfg.n_heads
+    inp = block_inputs(cfg)
+    mod, pos = h3.h3_build_packed_layout(cfg.n_text, cfg.video_t, cfg.video_h, cfg.video_w,
+                                         cfg.audio_channels, cfg.audio_steps)
+    x = inp["x"].to(dev)
+    wqkv, wo = inp["Wqkv"].to(dev), inp["Wo"].to(dev)
+    shift, scale, gate = inp["shift"].to(dev), inp["scale"].to(dev), inp["gate"].to(dev)
+    mod_d, pos_d = torch.from_numpy(mod).to(dev), torch.from_numpy(pos).to(dev)
+    n = max(args.steps, 3)
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        return a.elapsed_time(b) / n
+
+    res = {"context": "library", "config": {"workload": _workload(cfg), "L": L, "d": d,
+                                            "heads": H}, "steps": n, "h3": {}, "torch_sdpa": {},
+           "cublas": {}, "torch": torch.__version__}
+    qkv = None
+    for causal in (0, 1):
+        desc = h3.BlockDesc.make(L=L, d=d, n_heads=H, rope_sec=cfg.rope_sections,
+                                 rope_base=cfg.rope_base, ln_eps=cfg.ln_eps, n_mod=cfg.n_mod,
+                                 causal=causal)
+        nbytes = h3.h3_workspace_size(desc)
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        out = torch.empty(L, d, dtype=torch.bfloat16, device=dev)
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+        step = lambda: h3.h3_attn_block_fwd_profiled(desc, x, mod_d, pos_d, shift, scale, gate,
+                                                     wqkv, wo, ws, nbytes, out, evs, stream=stream)
+        block_ms = timed(step)
+        step()
+        torch.cuda.synchronize(dev)
+        attn_ms = evs[2].elapsed_time(evs[3])
+        flops = cfg.flops(causal=bool(causal))
+        attn_flops = 4.0 * d * (L * (L + 1) / 2.0 if causal else float(L) * L)
+        res["h3"]["causal" if causal else "full"] = {
+            "block_ms": block_ms, "block_tflops": flops / (block_ms * 1e-3) / 1e12,
+            "attention_ms_last_call": attn_ms,
+            "attention_tflops": attn_flops / (attn_ms * 1e-3) / 1e12}
+        if qkv is None:
+            off = (L * d * 2 + 255) // 256 * 256
+            qkv = ws[off:off + L * 3 * d * 2].view(torch.bfloat16).view(L, 3, H, 128).clone()
+        if h3.h3_sync_status(stream) != 0:
+            raise RuntimeError("device status after the block runs")
+        del ws, out
+    q, k, v = (qkv[:, i].permute(1, 0, 2).unsqueeze(0).contiguous() for i in range(3))
+    del qkv
+    try:
+        from torch.nn.attention import SDPBackend, sdpa_kernel
+        backends = {"cudnn": SDPBackend.CUDNN_ATTENTION, "flash": SDPBackend.FLASH_ATTENTION,
+                    "efficient": SDPBackend.EFFICIENT_ATTENTION}
+    except ImportError:
+        backends = {}
+    for name, be in backends.items():
+        for causal in (False, True):
+            key = f"{name}_{'causal' if causal else 'full'}"
+            try:
+                with sdpa_kernel([be]):
+                    ms = timed(lambda: F.scaled_dot_product_attention(q, k, v, is_causal=causal))
+                attn_flops = 4.0 * d * (L * (L + 1) / 2.0 if causal else float(L) * L)
+                res["torch_sdpa"][key] = {"ms": ms,
+                                          "tflops": attn_flops / (ms * 1e-3) / 1e12}
+            except Exception as e:   # a backend that does not support the shape or the GPU
+                res["torch_sdpa"][key] = {"unavailable": str(e).splitlines()[0][:160]}
+    del q, k, v
+    y = torch.randn(L, d, device=dev).to(torch.bfloat16)
+    for name, w in (("qkv_proj", wqkv), ("out_proj", wo)):
+        ms = timed(lambda: torch.matmul(y, w.t()))
+        res["cublas"][name] = {"ms": ms, "tflops": 2.0 * L * d * w.shape[0] / (ms * 1e-3) / 1e12}
+    print(json.dumps(res), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__,
                                  formatter_class=argparse.RawDescriptionHelpFormatter)
@@ -572,12 +667,17 @@ def main():
     ap.add_argument("--impl", default="h3", choices=["h3", "reference"])
     ap.add_argument("--config", default="full", help="block workload (default: full, L=58758)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--library-context", action="store_true",
+                    help="print this library's block next to PyTorch SDPA and cuBLAS on the "
+                         "same shapes (context; not the benchmark line)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)        # at least 3 untimed warm-up steps
     from h3inputs import CONFIGS
     cfg = CONFIGS[args.config]
     if args.impl == "reference":
         return run_reference(args, cfg)
+    if args.library_context:
+        return run_library_context(args, cfg)
     return run_gpu(args, cfg)
 
 
