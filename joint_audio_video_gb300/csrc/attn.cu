@@ -10,8 +10,10 @@
 //
 // One CTA = one head x 256 query rows, as two 128-row tiles Q0, Q1 that share
 // every K/V block fetched.  320 threads:
-//   warp 0      TMA producer: Q0|Q1 once, then K_j, V_j (128 x 128 bf16 each,
-//               two 64-column boxes with 128-byte swizzle) into a 4-slot ring
+//   warp 0      TMA producer: Q0|Q1 once, then per key block j the pair
+//               (K_j, V_{j-1}) that block's products read (128 x 128 bf16 tiles,
+//               two 64-column boxes with 128-byte swizzle) under one barrier,
+//               into two pair slots
 //   warp 1      TMEM owner + single-thread tcgen05.mma issuer
 //   warps 2..5  softmax warpgroup of tile 0 (one query row per thread)
 //   warps 6..9  softmax warpgroup of tile 1
@@ -41,11 +43,11 @@ namespace h3 {
 namespace {
 
 constexpr int kThreads = 320;
-constexpr int kStages = 4;
+constexpr int kSlots = 2;    // K/V pair slots of two tiles each (K_j, V_{j-1})
 constexpr uint32_t kTile = 128 * 128 * 2;     // one 128x128 bf16 tile (two 16 KB boxes)
 constexpr uint32_t kBox = 128 * 64 * 2;
 constexpr uint32_t kTile8 = 128 * 128;        // one 128x128 E4M3 tile (one 16 KB box)
-constexpr size_t kSmem = 2 * kTile + kStages * kTile + 1024;
+constexpr size_t kSmem = 2 * kTile + 2 * kSlots * kTile + 1024;
 constexpr float kRescaleThreshold = 8.0f;     // log2 units
 
 struct AttnDev {
@@ -189,7 +191,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm, const __grid_constant__ CUtensorMap tm8,
                     const __grid_constant__ AttnDev p) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t bar_q, bar_kv_full[kStages], bar_kv_empty[kStages], bar_s[2], bar_p[2],
+  __shared__ uint64_t bar_q, bar_kv_full[kSlots], bar_kv_empty[kSlots], bar_s[2], bar_p[2],
       bar_o, bar_drain;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
@@ -217,7 +219,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     abort_flag = 0;
     mbar_init(smem_u32(&bar_q), 1);
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kSlots; ++s) {
       mbar_init(smem_u32(&bar_kv_full[s]), 1);
       mbar_init(smem_u32(&bar_kv_empty[s]), 1);
     }
@@ -258,36 +260,43 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_2d(sQ + kTile, &tm, qb, xq, q0 + 128);
         tma_load_2d(sQ + kTile + kBox, &tm, qb, xq + 64, q0 + 128);
       }
-      int stage = 0;
-      uint32_t phase = 0;
+      // pair j = K_j (j < nblk) and V_{j-1} (j >= 1): the two tiles block j's
+      // products read, loaded under one barrier into slot j % 2 (K at the
+      // slot's start, V one tile further)
       bool ok = true;
-      for (int j = 0; j < nblk && ok; ++j) {
-        for (int kv = 0; kv < 2; ++kv) {
-          if (!mbar_wait(smem_u32(&bar_kv_empty[stage]), phase ^ 1u, wc)) { ok = false; break; }
-          const uint32_t fb = smem_u32(&bar_kv_full[stage]);
-          const uint32_t dst = sRing + stage * kTile;
-          const int x = kv == 0 ? xk : xv;
-          if (FP8 && kv == 0) {
-            mbar_arrive_expect_tx(fb, kTile8);
-            tma_load_2d(dst, &tm8, fb, x, kv_lo + j * 128);
-          } else {
-            mbar_arrive_expect_tx(fb, kTile);
-            tma_load_2d(dst, &tm, fb, x, kv_lo + j * 128);
-            tma_load_2d(dst + kBox, &tm, fb, x + 64, kv_lo + j * 128);
-          }
-          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+      int issued = 0;
+      for (int j = 0; j <= nblk && ok; ++j) {
+        const int slot = j & 1;
+        if (!mbar_wait(smem_u32(&bar_kv_empty[slot]), ((j >> 1) & 1) ^ 1u, wc)) {
+          ok = false;
+          break;
         }
+        const uint32_t fb = smem_u32(&bar_kv_full[slot]);
+        const uint32_t dst = sRing + slot * 2 * kTile;
+        const uint32_t kbytes = j < nblk ? (FP8 ? kTile8 : kTile) : 0u;
+        mbar_arrive_expect_tx(fb, kbytes + (j >= 1 ? kTile : 0u));
+        if (j < nblk) {
+          if (FP8) {
+            tma_load_2d(dst, &tm8, fb, xk, kv_lo + j * 128);
+          } else {
+            tma_load_2d(dst, &tm, fb, xk, kv_lo + j * 128);
+            tma_load_2d(dst + kBox, &tm, fb, xk + 64, kv_lo + j * 128);
+          }
+        }
+        if (j >= 1) {
+          tma_load_2d(dst + kTile, &tm, fb, xv, kv_lo + (j - 1) * 128);
+          tma_load_2d(dst + kTile + kBox, &tm, fb, xv + 64, kv_lo + (j - 1) * 128);
+        }
+        issued = j + 1;
       }
-      // let every copy in flight land before the CTA can exit
+      // let every copy in flight land before the CTA can exit (earlier pairs
+      // were consumed before their slot was refilled)
       WaitCtx drain{&abort_flag, p.status, 2000000ull};
       volatile int no_abort = 0;
       drain.abort = &no_abort;
-      if (!ok) {
-        for (int s = 0; s < kStages; ++s) {
-          const uint32_t par = (s < stage) ? phase : (phase ^ 1u);
-          mbar_wait(smem_u32(&bar_kv_full[s]), par, drain);
-        }
-      }
+      if (!ok)
+        for (int k = max(0, issued - 2); k < issued; ++k)
+          mbar_wait(smem_u32(&bar_kv_full[k & 1]), (k >> 1) & 1, drain);
       mbar_wait(qb, 0, drain);
     }
   } else if (warp == 1) {
@@ -297,65 +306,56 @@ __global__ void __launch_bounds__(kThreads, 1)
       // descriptors of Q0, Q1 and of every ring slot read as K (K-major) or V (MN-major)
       const SDesc dQ0 = sdesc_split(sdesc_sw128(sQ, 16, 1024));
       const SDesc dQ1 = sdesc_split(sdesc_sw128(sQ + kTile, 16, 1024));
-      // slots are kTile apart: a slot's descriptor is the first slot's plus s * kTile / 16
+      // pair slots are 2 kTile apart, V one kTile after K: a descriptor is the
+      // first slot's plus the byte offset / 16
       const SDesc dK0 = sdesc_split(sdesc_sw128(sRing, 16, 1024));
-      const SDesc dV0 = sdesc_split(sdesc_sw128(sRing, kBox, 1024));
-      auto dK = [&](uint32_t slot_idx) { return SDesc{dK0.lo + slot_idx * (kTile >> 4), dK0.hi}; };
-      auto dV = [&](uint32_t slot_idx) { return SDesc{dV0.lo + slot_idx * (kTile >> 4), dV0.hi}; };
-      auto slot = [&](int r, uint32_t& addr, uint32_t& par) {
-        addr = uint32_t(r % kStages);
-        par = (r / kStages) & 1;
-      };
-      auto kv_full = [&](int r) { return smem_u32(&bar_kv_full[r % kStages]); };
-      auto kv_empty = [&](int r) { return smem_u32(&bar_kv_empty[r % kStages]); };
+      const SDesc dV0 = sdesc_split(sdesc_sw128(sRing + kTile, kBox, 1024));
+      auto dK = [&](int j) { return SDesc{dK0.lo + uint32_t(j & 1) * (2 * kTile >> 4), dK0.hi}; };
+      auto dV = [&](int j) { return SDesc{dV0.lo + uint32_t(j & 1) * (2 * kTile >> 4), dV0.hi}; };
+      auto pair_full = [&](int j) { return smem_u32(&bar_kv_full[j & 1]); };
+      auto pair_empty = [&](int j) { return smem_u32(&bar_kv_empty[j & 1]); };
       const uint32_t tS0 = tmem, tS1 = tmem + 128, tO0 = tmem + 256, tO1 = tmem + 384;
-      uint32_t kA, kP, vA, vP;
-      if (ok) {
-        slot(0, kA, kP);
-        ok = mbar_wait(kv_full(0), kP, wc);
-      }
+      if (ok) ok = mbar_wait(pair_full(0), 0, wc);
       if (ok) {
         tc_fence_after();
-        s_product<FP8>(tS0, dQ0, dK(kA));
+        s_product<FP8>(tS0, dQ0, dK(0));
         tc_commit(smem_u32(&bar_s[0]));
-        s_product<FP8>(tS1, dQ1, dK(kA));
+        s_product<FP8>(tS1, dQ1, dK(0));
         tc_commit(smem_u32(&bar_s[1]));
-        tc_commit(kv_empty(0));
+        tc_commit(pair_empty(0));
       }
+      // block j: P(j-1).V_{j-1} and S(j) for each tile, both tiles from pair j
       for (int j = 1; j < nblk && ok; ++j) {
         const uint32_t pph = (j - 1) & 1;
-        slot(2 * j, kA, kP);
-        slot(2 * j - 1, vA, vP);
-        ok = mbar_wait(kv_full(2 * j), kP, wc) && mbar_wait(kv_full(2 * j - 1), vP, wc) &&
+        ok = mbar_wait(pair_full(j), (j >> 1) & 1, wc) &&
              mbar_wait(smem_u32(&bar_p[0]), pph, wc);
         if (!ok) break;
         tc_fence_after();
-        pv_product(tO0, tS0, dV(vA), j > 1);
-        s_product<FP8>(tS0, dQ0, dK(kA));
+        pv_product(tO0, tS0, dV(j), j > 1);
+        s_product<FP8>(tS0, dQ0, dK(j));
         tc_commit(smem_u32(&bar_s[0]));
         ok = mbar_wait(smem_u32(&bar_p[1]), pph, wc);
         if (!ok) break;
         tc_fence_after();
-        pv_product(tO1, tS1, dV(vA), j > 1);
-        tc_commit(kv_empty(2 * j - 1));
-        s_product<FP8>(tS1, dQ1, dK(kA));
+        pv_product(tO1, tS1, dV(j), j > 1);
+        s_product<FP8>(tS1, dQ1, dK(j));
         tc_commit(smem_u32(&bar_s[1]));
-        tc_commit(kv_empty(2 * j));
+        tc_commit(pair_empty(j));
       }
       if (ok) {
         const int j = nblk;
         const uint32_t pph = (j - 1) & 1;
-        slot(2 * j - 1, vA, vP);
-        ok = mbar_wait(kv_full(2 * j - 1), vP, wc) && mbar_wait(smem_u32(&bar_p[0]), pph, wc);
+        ok = mbar_wait(pair_full(j), (j >> 1) & 1, wc) &&
+             mbar_wait(smem_u32(&bar_p[0]), pph, wc);
         if (ok) {
           tc_fence_after();
-          pv_product(tO0, tS0, dV(vA), j > 1);
+          pv_product(tO0, tS0, dV(j), j > 1);
           ok = mbar_wait(smem_u32(&bar_p[1]), pph, wc);
         }
         if (ok) {
           tc_fence_after();
-          pv_product(tO1, tS1, dV(vA), j > 1);
-          tc_commit(kv_empty(2 * j - 1));
+          pv_product(tO1, tS1, dV(j), j > 1);
+          tc_commit(pair_empty(j));
           tc_commit(smem_u32(&bar_o));
         }
       }
