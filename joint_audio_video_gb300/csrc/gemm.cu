@@ -43,7 +43,7 @@ struct GemmCfg {
   static constexpr uint32_t kBBytes = BN * BK * 2;
   static constexpr uint32_t kStageBytes = kABytes + kBBytes;
   static constexpr uint32_t kTmemCols = 2 * BN;  // two accumulators
-  static constexpr size_t kSmem = size_t(kStages) * kStageBytes + 1024;
+  static constexpr size_t kSmem = size_t(kStages) * kStageBytes + 2 * BM * 64 + 1024;
 };
 
 struct GemmDev {
@@ -77,7 +77,8 @@ __device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int& mb
 template <int EPI, bool FP8>
 __device__ __forceinline__ void epilogue_chunk(const GemmDev& p, const RopeTable& rt,
                                                uint32_t (&r)[32], int grow, int gc,
-                                               const int32_t (&pr)[3], int m, float sa) {
+                                               const int32_t (&pr)[3], int m, float sa,
+                                               uint32_t (&pk)[16]) {
   float v[32];
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
@@ -117,7 +118,6 @@ __device__ __forceinline__ void epilogue_chunk(const GemmDev& p, const RopeTable
       v[i] = 0.5f * u * (1.f + tanhf(0.7978845608028654f * fmaf(0.044715f * u, u * u, u)));
     }
   }
-  __nv_bfloat16* crow = p.C + size_t(grow) * p.N + gc;
   if constexpr (EPI == EPI_GATED_RESIDUAL) {
     const uint4* xr = reinterpret_cast<const uint4*>(p.x_res + size_t(grow) * p.N + gc);
     const float4* gr = reinterpret_cast<const float4*>(p.gate + size_t(m) * p.N + gc);
@@ -135,18 +135,51 @@ __device__ __forceinline__ void epilogue_chunk(const GemmDev& p, const RopeTable
       v[4 * i + 3] = fmaf(g.w, v[4 * i + 3], __uint_as_float(w1 & 0xFFFF0000u));
     }
   }
-  uint4* out = reinterpret_cast<uint4*>(crow);
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    out[i] = make_uint4(pack_bf16x2(v[8 * i + 0], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
-                        pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
-  }
+  for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+}
+
+// The epilogue hands C to the TMA in 128-row x 32-column chunks staged in shared
+// memory (64-byte rows with the 64-byte swizzle: 16-byte chunk c of row r at
+// c ^ ((r / 2) % 4)), two staging buffers; each chunk is one bulk tensor store,
+// so C leaves the SM as whole lines instead of one 16-byte piece per row.
+constexpr uint32_t kStageC = BM * 64;   // bytes of one staging buffer
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int32_t x,
+                                             int32_t y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(src), "r"(x), "r"(y)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// At most one committed store group may still be reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_1() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+__device__ __forceinline__ void epi_bar() {   // the 128 epilogue threads
+  asm volatile("bar.sync 1, 128;" ::: "memory");
+}
+__device__ __forceinline__ bool epi_bar_and(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred q, a;\n\tsetp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.and.pred a, 1, 128, q;\n\tselp.u32 %0, 1, 0, a;\n\t}"
+      : "=r"(r)
+      : "r"(uint32_t(pred))
+      : "memory");
+  return r != 0;
 }
 
 template <int BN, int EPI, bool FP8>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const __grid_constant__ GemmDev p, const __grid_constant__ RopeTable rt) {
+                const __grid_constant__ CUtensorMap tmC, const __grid_constant__ GemmDev p,
+                const __grid_constant__ RopeTable rt) {
   using Cfg = GemmCfg<BN>;
   constexpr int S = Cfg::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -178,6 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane_id() == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmC);
   }
   tc_fence_before();
   __syncthreads();
@@ -266,13 +300,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------------- epilogue
     const int q = warp & 3;                 // TMEM lane quarter of this warp
     const int row_in_tile = q * 32 + lane_id();
+    const bool leader = threadIdx.x == 64;   // issues the C stores
+    const uint32_t sC = base + S * Cfg::kStageBytes;
+    const uint32_t srow = uint32_t(row_in_tile) * 64;
+    const uint32_t ssw = uint32_t(row_in_tile >> 1) & 3u;
+    int chunk = 0;                           // C chunks staged so far (buffer parity)
     int it = 0;
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++it) {
       int mb, nb;
       tile_coords(t, p.num_m, p.num_n, mb, nb);
       const int acc = it & 1;
       const uint32_t acc_phase = (it >> 1) & 1;
-      const bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_acc_full[acc]), acc_phase, wc));
+      // all four epilogue warps leave together (they share the staging barrier)
+      const bool ok = epi_bar_and(mbar_wait(smem_u32(&bar_acc_full[acc]), acc_phase, wc));
       if (!ok) break;
       tc_fence_after();
       const int grow = mb * BM + row_in_tile;
@@ -303,18 +343,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t r[32];
         tmem_ld32(tacc + c * 32, r);
         tmem_ld_wait(r);
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) pk[i] = 0u;   // rows past M: clipped by the store
         if (live) {
           if (bad) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) r[i] = 0x7FC00000u;   // NaN row
           }
-          epilogue_chunk<EPI, FP8>(p, rt, r, grow, nb * BN + c * 32, pr, m, sa);
+          epilogue_chunk<EPI, FP8>(p, rt, r, grow, nb * BN + c * 32, pr, m, sa, pk);
         }
+        // the store that last read this buffer (two chunks ago) has read it
+        const uint32_t sb = sC + uint32_t(chunk & 1) * kStageC;
+        if (leader) bulk_wait_read_1();
+        epi_bar();
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(sb + srow + ((uint32_t(i) ^ ssw) << 4)),
+                       "r"(pk[4 * i]), "r"(pk[4 * i + 1]), "r"(pk[4 * i + 2]), "r"(pk[4 * i + 3])
+                       : "memory");
+        fence_async_shared();
+        epi_bar();
+        if (leader) {
+          tma_store_2d(&tmC, sb, nb * BN + c * 32, mb * BM);
+          bulk_commit();
+        }
+        ++chunk;
       }
       if (bad) atomicCAS(p.status, H3_DEV_OK, H3_DEV_BAD_INDEX);
       tc_fence_before();
       mbar_arrive(smem_u32(&bar_acc_empty[acc]));
     }
+    // every C store has finished before the CTA (and its shared memory) goes away
+    if (leader) bulk_wait_all();
   }
 
   tc_fence_before();
@@ -334,6 +395,8 @@ cudaError_t launch_typed(const GemmArgs& a, const DevCtx& ctx, cudaStream_t st) 
     if (!make_tmap_bf16_2d(&tmA, a.A, a.M, a.K, a.K, BM, BK)) return cudaErrorInvalidValue;
     if (!make_tmap_bf16_2d(&tmB, a.B, a.N, a.K, a.K, BN, BK)) return cudaErrorInvalidValue;
   }
+  CUtensorMap tmC;
+  if (!make_tmap_bf16_2d_sw64(&tmC, a.C, a.M, a.N, a.N, BM)) return cudaErrorInvalidValue;
   GemmDev p{};
   p.C = static_cast<__nv_bfloat16*>(a.C);
   p.M = a.M;
@@ -359,7 +422,7 @@ cudaError_t launch_typed(const GemmArgs& a, const DevCtx& ctx, cudaStream_t st) 
   if (e != cudaSuccess) return e;
   const int tiles = p.num_m * p.num_n;
   const int grid = tiles < ctx.num_sms ? tiles : ctx.num_sms;
-  kern<<<grid, kThreads, Cfg::kSmem, st>>>(tmA, tmB, p, rt);
+  kern<<<grid, kThreads, Cfg::kSmem, st>>>(tmA, tmB, tmC, p, rt);
   return cudaGetLastError();
 }
 
