@@ -291,7 +291,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // let every copy in flight land before the CTA can exit (earlier pairs
       // were consumed before their slot was refilled)
-      WaitCtx drain{&abort_flag, p.status, 2000000ull};
+      WaitCtx drain{&abort_flag, p.status, kDrainWaitNs};
       volatile int no_abort = 0;
       drain.abort = &no_abort;
       if (!ok)
@@ -360,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       tc_commit(smem_u32(&bar_drain));
-      WaitCtx drain{&abort_flag, p.status, p.wait_ns};
+      WaitCtx drain{&abort_flag, p.status, kDrainWaitNs};
       volatile int no_abort = 0;
       drain.abort = &no_abort;
       mbar_wait(smem_u32(&bar_drain), 0, drain);

@@ -246,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) {
         // unwind: let copies already in flight land before the CTA exits
-        WaitCtx drain{&abort_flag, p.status, 2000000ull};
+        WaitCtx drain{&abort_flag, p.status, kDrainWaitNs};
         volatile int no_abort = 0;
         drain.abort = &no_abort;
         for (int s = 0; s < S; ++s) {
@@ -294,7 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // drain: every MMA issued so far has finished before TMEM is released
       tc_commit(smem_u32(&bar_drain));
-      WaitCtx drain{&abort_flag, p.status, p.wait_ns};
+      WaitCtx drain{&abort_flag, p.status, kDrainWaitNs};
       volatile int no_abort = 0;
       drain.abort = &no_abort;
       mbar_wait(smem_u32(&bar_drain), 0, drain);

@@ -57,6 +57,12 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Bound of the waits that let a CTA's own in-flight copies and MMAs finish
+// before it releases shared or tensor memory on the way out (they complete in
+// microseconds).  Fixed, so that a short caller-set wait limit can never free
+// tensor memory under a running MMA.
+constexpr uint64_t kDrainWaitNs = 200000000ull;
+
 // Per-CTA context of a bounded wait.
 struct WaitCtx {
   volatile int* abort;   // shared-memory flag, raised by the first warp that gives up
