@@ -41,6 +41,15 @@ def _workload(cfg) -> str:
             f"full attention, batch 1")
 
 
+def _config(cfg, world: int = 1) -> dict:
+    """The workload description both arms print (same keys, same values)."""
+    return {"workload": _workload(cfg), "L": cfg.L, "d": cfg.d, "heads": cfg.n_heads,
+            "causal": False,
+            "l2": f"inputs larger than L2 (x {cfg.L * cfg.d * 2 / 1e6:.0f} MB, qkv "
+                  f"{cfg.L * 3 * cfg.d * 2 / 1e9:.2f} GB per step)",
+            "parallelism": f"replicas x{world}"}
+
+
 def _peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -186,7 +195,7 @@ def run_reference(args, cfg):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": full * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": _workload(cfg), "L": cfg.L, "d": cfg.d, "heads": cfg.n_heads},
+        "config": _config(cfg, args.gpus),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -373,6 +382,20 @@ def run_gpu(args, cfg):
     varlen_flops = 4.0 * d * sum((cu[i + 1] - cu[i]) ** 2 for i in range(3))
     del o_var
 
+    # ---- the standalone 3D RoPE call (h3_mrope_apply, in place on Q and K of the
+    # workspace's qkv; the fused block applies RoPE in the QKV epilogue instead).
+    # Its 2.4 GB of traffic per call exceed L2, so no flush is needed.
+    for _ in range(2):
+        h3.h3_mrope_apply(qkv_ws, pos_d, L, H, stream=stream)
+    rev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    rev[0].record(stream)
+    for _ in range(10):
+        h3.h3_mrope_apply(qkv_ws, pos_d, L, H, stream=stream)
+    rev[1].record(stream)
+    torch.cuda.synchronize(dev)
+    mrope_ms = rev[0].elapsed_time(rev[1]) / 10
+    mrope_bytes = 8.0 * L * d + 12.0 * L
+
     # ---- the MLP sub-block of the same layer (hidden 4d), timed on its own
     hid = 4 * d
     gmlp = torch.Generator(device="cpu").manual_seed(11)
@@ -500,23 +523,33 @@ def run_gpu(args, cfg):
         # counters taken on another version of the kernel do not describe this one
         traffic = rec.get("bytes_per_launch_full") if same else None
 
+    # the peak's own clock: the sustained GEMM loop ran under the power cap at a
+    # lower SM clock than a kernel inside this step, so the fraction is also
+    # given against that peak scaled to the kernel's clock
+    peak_mhz = None
+    if isinstance(peaks.get("clocks_under_load"), dict):
+        peak_mhz = peaks["clocks_under_load"].get("sm_mhz_median")
+    run_mhz = clocks.get("sm_mhz") if clocks else None
+    frac_clk = (achieved / (peak * run_mhz / peak_mhz)
+                if peak_mhz and run_mhz else None)
+    mcycles = ({n: t * run_mhz / 1e3 for n, t in per.items()} if run_mhz else None)
+    hbm = float(peaks["hbm_gbs"])
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": _workload(cfg),
-                   "L": L, "d": d, "heads": H, "causal": False,
-                   "l2": f"inputs larger than L2 (x {L * d * 2 / 1e6:.0f} MB, qkv "
-                         f"{L * 3 * d * 2 / 1e9:.2f} GB per step)",
-                   "parallelism": f"replicas x{world}"},
+        "config": _config(cfg, world),
         "tokens_per_s": job_throughput(L, world, ms),
         "pct_of_bf16_peak_block": flops / (ms * 1e-3) / 1e12 / peak,
         "kernel_ms": per,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic,
+                     "frac_at_kernel_clock": frac_clk,
+                     "peak_sm_mhz": peak_mhz, "kernel_sm_mhz": run_mhz,
                      "kernel": "attention (attn_fwd_kernel)",
                      "peak_kind": f"{peak_kind} bf16 sustained (kernel inside a long step)"},
+        "kernel_mcycles": mcycles,
         "e2e": {"value": job_throughput(flops, world, e2e_ms) / 1e12, "unit": UNIT,
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "sweep50": {"steps": 50, "total_ms": sweep_total,
@@ -542,10 +575,15 @@ def run_gpu(args, cfg):
                 "note": "projections in E4M3 (tcgen05 kind::f8f6f4); attention scores from "
                         "E4M3 Q and K, P.V in bf16; attention_ms includes the Q/K "
                         "quantisation; FLOPs counted as for the bf16 block"},
+        "mrope_standalone": {"ms": mrope_ms, "bytes": mrope_bytes,
+                             "gbs": mrope_bytes / (mrope_ms * 1e-3) / 1e9,
+                             "frac_of_hbm_peak": mrope_bytes / (mrope_ms * 1e-3) / 1e9 / hbm},
+        "modulate_hbm": {"ms": per["modulate"], "bytes": 4.0 * L * d,
+                         "gbs": 4.0 * L * d / (per["modulate"] * 1e-3) / 1e9,
+                         "frac_of_hbm_peak": 4.0 * L * d / (per["modulate"] * 1e-3) / 1e9 / hbm},
         "denoise_step": {"L": L, "C": C_lat, "ms": denoise_ms,
                          "gbs": denoise_bytes / (denoise_ms * 1e-3) / 1e9,
-                         "frac_of_hbm_peak": denoise_bytes / (denoise_ms * 1e-3) / 1e9
-                         / float(peaks["hbm_gbs"])},
+                         "frac_of_hbm_peak": denoise_bytes / (denoise_ms * 1e-3) / 1e9 / hbm},
         "gpu_launches": 4 * args.steps,
         "clocks": clocks,
         "wall_s_timed": wall,

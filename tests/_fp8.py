@@ -26,3 +26,55 @@ def e4m3_round(t: np.ndarray) -> np.ndarray:
     d_lo, d_hi = a - _POS[lo], _POS[hi] - a
     code = np.where(d_lo < d_hi, lo, np.where(d_hi < d_lo, hi, np.where(lo % 2 == 0, lo, hi)))
     return (code | (np.signbit(t).astype(np.int64) << 7)).astype(np.uint8)
+
+
+_F448 = np.float32(448.0)
+
+
+def codes_and_scale(x32: np.ndarray, amax: np.ndarray):
+    """E4M3 codes of float32 values ``x32`` that share the maxima ``amax``
+    (broadcast against x32), and the group scales amax / 448 (1 for an
+    all-zero group).  Both decisions are taken in float32, the precision the
+    quantising kernels take them in: x * (448 / amax) rounded to the nearest
+    code, ties to even, saturating."""
+    x32 = np.asarray(x32, dtype=np.float32)
+    amax = np.asarray(amax, dtype=np.float32)
+    nz = amax > 0
+    scale = np.where(nz, amax / _F448, np.float32(1.0)).astype(np.float32)
+    inv = np.where(nz, _F448 / np.where(nz, amax, np.float32(1.0)),
+                   np.float32(1.0)).astype(np.float32)
+    return scale, e4m3_round((x32 * inv).astype(np.float32))
+
+
+def quantize_rows(x: np.ndarray):
+    """Row-wise quantisation of ``x [R, K]``: (codes [R, K], scales [R])."""
+    x32 = np.asarray(x, dtype=np.float32)
+    s, q = codes_and_scale(x32, np.abs(x32).max(axis=1, keepdims=True))
+    return q, s[:, 0]
+
+
+def dequant_rows(x: np.ndarray) -> np.ndarray:
+    """The float64 values a row-quantised operand stands for: code x scale."""
+    q, s = quantize_rows(x)
+    return e4m3_decode(q) * s.astype(np.float64)[:, None]
+
+
+def dequant_qk(qkv: np.ndarray, n_heads: int, head_dim: int = 128, block: int = 128
+               ) -> np.ndarray:
+    """``qkv [L, 3*H*dh]`` with Q replaced by its per-token E4M3 values and K by
+    its per-(head, 128-key block) E4M3 values, times their scales; V as is."""
+    x = np.asarray(qkv, dtype=np.float32)
+    L, d = x.shape[0], n_heads * head_dim
+    nb = (L + block - 1) // block
+    out = np.asarray(qkv, dtype=np.float64).copy()
+    for h in range(n_heads):
+        cq = slice(h * head_dim, (h + 1) * head_dim)
+        out[:, cq] = dequant_rows(x[:, cq])
+        # K blocks of 128 keys (the last one padded with zeros, which change no maximum)
+        k = np.zeros((nb * block, head_dim), dtype=np.float32)
+        k[:L] = x[:, d + h * head_dim:d + (h + 1) * head_dim]
+        kb = k.reshape(nb, block * head_dim)
+        s, q = codes_and_scale(kb, np.abs(kb).max(axis=1, keepdims=True))
+        deq = e4m3_decode(q) * s.astype(np.float64)
+        out[:, d + h * head_dim:d + (h + 1) * head_dim] = deq.reshape(nb * block, head_dim)[:L]
+    return out

@@ -20,6 +20,15 @@ def to64(t) -> np.ndarray:
 # against 2e-2*RMS + 2^-8*|ref|; the block output keeps the plain bound.
 BF16_U = 2.0 ** -8
 
+# Inside the fused block, O and the branch O Wo^T also carry the bf16 storage
+# of y and of the rotated q, k, v: every logit moves by about one bf16 rounding
+# against the fp64 chain.  An exactly rounded chain (y, qkv and O stored in
+# bf16, P rounded to bf16 before P.V, everything else exact) reaches
+# 3.06e-2 x RMS above the 2^-8 |ref| term on the branch over 40 seeds of the
+# tiny workload (test_chain_bound_cpu.py recomputes it), so a kernel cannot be
+# held to the plain 2e-2 there; the chain bound is that measurement plus 30 %.
+CHAIN_MAX_REL_RMS = 4e-2
+
 
 def stats(got: np.ndarray, ref: np.ndarray):
     got = np.asarray(got, dtype=np.float64)
@@ -53,3 +62,15 @@ def assert_parity(got, ref, what: str, max_rel_rms: float = MAX_REL_RMS,
         f"{' + 2^-8|ref|' if bf16_storage else ''}, worst excess {excess:.3e}), "
         f"mean rel = {mr:.3e} (<= {mean_rel})")
     return mx, mr
+
+
+def slice_rows(L: int, n_text: int) -> np.ndarray:
+    """The 1,024 query rows of the full-size spot check: rows 0..127 (text),
+    one video row every 75 tokens from the first video token (768 rows that
+    span every latent frame t), and the last 128 rows (audio, including the
+    6-row ragged tail that a 128-row tiling leaves at L = 58,758)."""
+    video = n_text + 75 * np.arange(768)
+    assert video[-1] < L - 128, "the slice protocol needs the full-size workload"
+    rows = np.concatenate([np.arange(128), video, np.arange(L - 128, L)])
+    assert len(np.unique(rows)) == 1024
+    return rows.astype(np.int64)

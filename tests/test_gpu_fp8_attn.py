@@ -26,8 +26,8 @@ import torch
 
 import oracle as orc
 from h3inputs import CONFIGS, attention_qkv
-from tests._fp8 import e4m3_decode, e4m3_round
-from tests._parity import assert_parity, to64
+from tests._fp8 import codes_and_scale, dequant_qk, e4m3_decode
+from tests._parity import assert_parity, slice_rows, to64
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -51,15 +51,6 @@ def _quantize(h3, qkv, L, H):
     return qk8.cpu().numpy(), sq.cpu().numpy(), sk.cpu().numpy()
 
 
-def _codes_and_scale(x32: np.ndarray, amax: np.ndarray):
-    """Expected scale and codes for float32 values x32 grouped with maxima amax."""
-    f448 = np.float32(448.0)
-    nz = amax > 0
-    scale = np.where(nz, amax / f448, np.float32(1.0)).astype(np.float32)
-    inv = np.where(nz, f448 / np.where(nz, amax, 1), np.float32(1.0)).astype(np.float32)
-    return scale, e4m3_round(x32 * inv)
-
-
 def _same_codes(got: np.ndarray, want: np.ndarray) -> bool:
     # +0 and -0 are the same value
     g = np.where((got & 0x7F) == 0, 0, got)
@@ -79,13 +70,13 @@ def test_quantize_qk_codes_and_scales_bit_exact(h3, L, H):
     nkb = (L + 127) // 128
     for h in range(H):
         q = x[:, h * 128:(h + 1) * 128]
-        s_want, c_want = _codes_and_scale(q, np.abs(q).max(axis=1, keepdims=True))
+        s_want, c_want = codes_and_scale(q, np.abs(q).max(axis=1, keepdims=True))
         assert np.array_equal(sq[h], s_want[:, 0]), f"Q scales, head {h}"
         assert _same_codes(qk8[:, h * 128:(h + 1) * 128], c_want), f"Q codes, head {h}"
         k = x[:, d + h * 128:d + (h + 1) * 128]
         for b in range(nkb):
             kb = k[b * 128:(b + 1) * 128]
-            s_want, c_want = _codes_and_scale(kb, np.abs(kb).max(keepdims=True))
+            s_want, c_want = codes_and_scale(kb, np.abs(kb).max(keepdims=True))
             assert sk[h, b] == s_want.reshape(-1)[0], f"K scale, head {h} block {b}"
             got = qk8[b * 128:(b + 1) * 128, d + h * 128:d + (h + 1) * 128]
             assert _same_codes(got, c_want), f"K codes, head {h} block {b}"
@@ -96,25 +87,8 @@ def test_quantize_qk_codes_and_scales_bit_exact(h3, L, H):
     assert np.abs(e4m3_decode(qk8[:, :128])).max() == 448.0
 
 
-def _quantized_oracle_input(qkv, H):
-    """qkv with Q and K replaced by their E4M3 values times their scales."""
-    x = qkv.float().numpy()
-    L, d = x.shape[0], H * 128
-    out = x.astype(np.float64)
-    for h in range(H):
-        c = slice(h * 128, (h + 1) * 128)
-        s, code = _codes_and_scale(x[:, c], np.abs(x[:, c]).max(axis=1, keepdims=True))
-        out[:, c] = e4m3_decode(code) * s
-        ck = slice(d + h * 128, d + (h + 1) * 128)
-        for b in range(0, L, 128):
-            kb = x[b:b + 128, ck]
-            s, code = _codes_and_scale(kb, np.abs(kb).max(keepdims=True))
-            out[b:b + 128, ck] = e4m3_decode(code) * s
-    return out
-
-
 def _check(O, qkv, H, causal, what, lse=None, exact=True):
-    oq, lq = orc.attention(_quantized_oracle_input(qkv, H), H, 128, causal=bool(causal))
+    oq, lq = orc.attention(dequant_qk(qkv.float().numpy(), H), H, 128, causal=bool(causal))
     assert_parity(to64(O), oq, what + " vs quantised-input oracle")
     if lse is not None:
         np.testing.assert_allclose(to64(lse), lq, atol=2e-2, rtol=1e-3)
@@ -165,7 +139,7 @@ def test_attention_fp8_identical_keys_give_mean_of_values(h3):
     assert_parity(to64(O), np.tile(want, (L, 1)), "fp8 identical keys")
 
 
-def test_attention_fp8_full_size_sampled_rows(h3):
+def test_attention_fp8_full_size_slice_rows(h3):
     c = CONFIGS["full"]
     L, H = c.L, c.n_heads
     qkv = attention_qkv(L, H, seed=59)
@@ -174,9 +148,10 @@ def test_attention_fp8_full_size_sampled_rows(h3):
     h3.h3_joint_attn_fwd_fp8(qkv.to(DEV), L, H, 128, 0, 1 / math.sqrt(128), ws, n, O)
     assert h3.h3_sync_status() == 0
     assert torch.isfinite(O.float()).all()
-    rows = np.unique(np.concatenate([np.arange(0, 4), np.arange(L - 8, L),
-                                     np.linspace(0, L - 1, 40).astype(np.int64)]))
-    ro, _ = orc.attention(to64(qkv), H, 128, rows=rows)
+    rows = slice_rows(L, c.n_text)
     ridx = torch.from_numpy(rows).to(DEV)
-    assert_parity(to64(O[ridx]), ro, "fp8 full-size attention rows", max_rel_rms=SCORE_MAX,
-                  mean_rel=FP8_MEAN)
+    oq, _ = orc.attention(dequant_qk(qkv.float().numpy(), H), H, 128, rows=rows)
+    assert_parity(to64(O[ridx]), oq, "fp8 full-size attention, slice rows, vs quantised-input oracle")
+    ro, _ = orc.attention(to64(qkv), H, 128, rows=rows)
+    assert_parity(to64(O[ridx]), ro, "fp8 full-size attention, slice rows, vs exact",
+                  max_rel_rms=SCORE_MAX, mean_rel=FP8_MEAN)

@@ -7,9 +7,11 @@ each of the 50 denoising steps; §4 Denoising Execution Flow).
 The oracle runs its own 50-step chain (float64 inside a step, the step's
 output stored as bf16 - the block's input/output type - before it becomes the
 next input) at the tiny size and is compared at steps 1, 25 and 50.  At full
-size the sweep is checked through properties that hold at any size: finite
-outputs, bitwise determinism, and a sweep step equal to a standalone call of
-the block on the same input.
+size the oracle takes the input of steps 1, 25 and 50 exactly as the GPU
+consumed it (a bf16 state, like a seeded draw), computes that step itself on
+the 1,024-row slice (keys and values of every token), and the step's output,
+rotated qkv and O are compared with it; errors therefore do not compound
+across steps, and every expected value is the oracle's own.
 """
 import numpy as np
 import pytest
@@ -18,6 +20,7 @@ import torch
 import oracle as orc
 from h3inputs import CONFIGS, block_inputs, sweep_modulation
 from tests._parity import assert_parity, to64
+from tests.test_gpu_fullsize import check_full_block_slice
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -48,9 +51,13 @@ def _step(h3, desc, nbytes, dev, k, x, out):
                          dev["Wqkv"], dev["Wo"], dev["ws"], nbytes, out)
 
 
-def _sweep(h3, desc, nbytes, dev, keep=CHECK):
-    """Run the sweep in place on dev['x']; return copies of the states at `keep`."""
+def _sweep(h3, desc, nbytes, dev, keep=CHECK, inner=False):
+    """Run the sweep in place on a copy of dev['x']; return copies of the
+    states at `keep` (and, with `inner`, of the rotated qkv and O those steps
+    left in the workspace)."""
     x = dev["x"].clone()
+    L, d = desc.L, desc.d
+    off = (L * d * 2 + 255) // 256 * 256
     saved = {}
     for k in range(1, STEPS + 1):
         if k in keep:
@@ -58,6 +65,10 @@ def _sweep(h3, desc, nbytes, dev, keep=CHECK):
         _step(h3, desc, nbytes, dev, k, x, x)          # out aliases x
         if k in keep:
             saved[k] = x.clone()
+            if inner:
+                saved[f"O{k}"] = dev["ws"][:L * d * 2].view(torch.bfloat16).view(L, d).clone()
+                saved[f"qkv{k}"] = dev["ws"][off:off + L * 3 * d * 2].view(
+                    torch.bfloat16).view(L, 3 * d).clone()
     assert h3.h3_sync_status() == 0
     return saved
 
@@ -86,20 +97,21 @@ def test_sweep_tiny_against_oracle_chain(h3):
                               roundings=3.0 * np.sqrt(k - 1))
 
 
-def test_sweep_full_size_properties(h3):
+def test_sweep_full_size_against_oracle_slice(h3):
     c = CONFIGS["full"]
     inp, desc, nbytes, dev = _setup(h3, c)
-    a = _sweep(h3, desc, nbytes, dev)
+    a = _sweep(h3, desc, nbytes, dev, inner=True)
+    omod, opos = orc.packed_layout(c.n_text, c.video_t, c.video_h, c.video_w,
+                                   c.audio_channels, c.audio_steps)
+    wqkv, wo = to64(inp["Wqkv"]), to64(inp["Wo"])
     for k in CHECK:
-        assert torch.isfinite(a[k].float()).all(), f"non-finite output at step {k}"
-    # the state moves: each checked step differs from its input
-    for k in CHECK:
+        # the state moves: each checked step differs from its input
         assert not torch.equal(a[k], a[f"in{k}"])
+        m64 = {n: v.double().numpy() for n, v in sweep_modulation(c, k).items()}
+        check_full_block_slice(c, to64(a[f"in{k}"]), omod, opos, m64, wqkv, wo, a[k],
+                               a[f"qkv{k}"], a[f"O{k}"], f"sweep step {k}")
+        for n in (f"O{k}", f"qkv{k}"):
+            del a[n]
     # bitwise deterministic
     b = _sweep(h3, desc, nbytes, dev, keep=(50,))
     assert torch.equal(a[50], b[50])
-    # step 25 of the sweep equals a standalone call on its saved input
-    out = torch.empty_like(a[25])
-    _step(h3, desc, nbytes, dev, 25, a["in25"], out)
-    assert h3.h3_sync_status() == 0
-    assert torch.equal(out, a[25])
