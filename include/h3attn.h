@@ -46,6 +46,16 @@
  *   - A kernel that finds an out-of-range modality id or gives up on a
  *     bounded wait records it in a per-device status word; h3_sync_status()
  *     reports and clears it.  No C++ exception crosses this boundary.
+ *   - With H3_DEBUG_SYNC=1 in the environment (read once per process), every
+ *     call that launches work waits for its stream before returning and
+ *     returns what h3_sync_status() would, so an error surfaces at the call
+ *     that caused it; a stream that is being captured is not waited on.
+ *   - Every call that launches work opens an NVTX range named after itself
+ *     around its host-side work (visible to a timeline profiler).
+ *   - The library looks up the device addresses of its own device variables
+ *     once per device and keeps them: cudaDeviceReset() on a device while the
+ *     library is loaded is not supported (the kept addresses would point
+ *     into the destroyed context); restart the process instead.
  */
 #ifndef H3ATTN_H_
 #define H3ATTN_H_
@@ -359,8 +369,11 @@ h3_status h3_attn_block_fwd_profiled(const h3_block_desc* desc, const uint16_t* 
  *     exceeds H3_NOALLOC_SCRATCH_BYTES (e.g. 4,096 tokens at d = 2048 fit
  *     exactly; 58,758 tokens at d = 5120 do not).
  *   - The first call on a device looks up the workspace's device address
- *     (cudaGetSymbolAddress) with that device current: make it before any
- *     stream capture begins.
+ *     (cudaGetSymbolAddress) with that device current.  With CUDA's lazy
+ *     module loading that lookup is also when the 64 MiB are reserved on the
+ *     device, so make the first call during set-up: before the caller's
+ *     allocator or engine takes the device's memory, and before any stream
+ *     capture begins.
  *   - All calls on a device share the one workspace and it keeps the last
  *     call's contents (nothing in it needs to start at zero).  Calls that
  *     overlap on the GPU race on it: order them on one stream or with events.

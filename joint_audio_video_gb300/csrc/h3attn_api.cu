@@ -5,10 +5,12 @@
 // Kernels report asynchronous problems (bounded wait ran out, modality id out
 // of range) through one status word per device, read by h3_sync_status().
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <atomic>
 #include <cmath>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 
 #include "../../include/h3attn.h"
@@ -25,6 +27,9 @@ constexpr uint64_t kDefaultWaitNs = 2000000000ull;
 constexpr int kMaxDevices = 64;
 std::atomic<uint64_t> g_wait_ns{kDefaultWaitNs};
 
+// Per device: the status word's device address and the SM count, looked up
+// once and kept (a cudaDeviceReset() while the library is loaded is not
+// supported: the address would point into the destroyed context).
 struct DevInfo {
   std::atomic<int> ready{0};
   int* status = nullptr;
@@ -63,6 +68,45 @@ bool overlap(const void* a, size_t na, const void* b, size_t nb) {
 bool valid_d(int32_t d) { return d >= 128 && d <= 16384 && d % 128 == 0; }
 
 h3_status launched(cudaError_t e) { return e == cudaSuccess ? H3_OK : H3_ERR_CUDA; }
+
+// An NVTX range named after the entry point around its host-side work, so a
+// timeline tool shows which call enqueued which kernels.
+struct Trace {
+  explicit Trace(const char* name) { nvtxRangePushA(name); }
+  ~Trace() { nvtxRangePop(); }
+  Trace(const Trace&) = delete;
+  Trace& operator=(const Trace&) = delete;
+};
+
+// H3_DEBUG_SYNC=1 (read once per process): every entry point that launches
+// work waits for its stream before returning and returns the device status,
+// so an asynchronous fault or a kernel-reported error (timeout, bad modality
+// id) surfaces at the call that caused it.  A stream that is being captured
+// is not waited on.
+bool debug_sync() {
+  static const bool on = [] {
+    const char* e = std::getenv("H3_DEBUG_SYNC");
+    return e != nullptr && e[0] == '1' && e[1] == '\0';
+  }();
+  return on;
+}
+
+}  // namespace
+}  // namespace h3
+
+extern "C" h3_status h3_sync_status(h3_stream_t stream);
+
+namespace h3 {
+namespace {
+
+h3_status finish(h3_status s, h3_stream_t stream) {
+  if (s != H3_OK || !debug_sync()) return s;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(reinterpret_cast<cudaStream_t>(stream), &cap) != cudaSuccess)
+    return H3_ERR_CUDA;
+  if (cap != cudaStreamCaptureStatusNone) return s;
+  return h3_sync_status(stream);
+}
 
 h3_status check_rope(const int32_t sec[3], int32_t head_dim, float base) {
   if (sec == nullptr) return H3_ERR_INVALID_ARG;
@@ -137,6 +181,7 @@ void h3_set_wait_limit_ns(uint64_t limit_ns) {
 h3_status h3_adaln_modulate(const uint16_t* x, const uint8_t* mod, const float* shift,
                             const float* scale, int32_t L, int32_t d, int32_t n_mod, float eps,
                             uint16_t* y, h3_stream_t stream) {
+  const Trace trace_("h3_adaln_modulate");
   if (L < 1 || !valid_d(d) || n_mod < 1 || n_mod > 255) return H3_ERR_INVALID_ARG;
   if (!(eps >= 0.f) || !std::isfinite(eps)) return H3_ERR_INVALID_ARG;
   if (!aligned16(x) || mod == nullptr || !aligned16(shift) || !aligned16(scale) || !aligned16(y))
@@ -145,12 +190,13 @@ h3_status h3_adaln_modulate(const uint16_t* x, const uint8_t* mod, const float* 
   if (x != y && overlap(x, bytes, y, bytes)) return H3_ERR_INVALID_ARG;
   DevCtx ctx;
   if (h3_status s = dev_ctx(&ctx)) return s;
-  return launched(launch_adaln_modulate(x, mod, shift, scale, L, d, n_mod, eps, y, ctx,
-                                        reinterpret_cast<cudaStream_t>(stream)));
+  return finish(launched(launch_adaln_modulate(x, mod, shift, scale, L, d, n_mod, eps, y, ctx,
+                                        reinterpret_cast<cudaStream_t>(stream))), stream);
 }
 
 h3_status h3_qkv_proj(const uint16_t* y, const uint16_t* Wqkv, int32_t L, int32_t d, uint16_t* qkv,
                       h3_stream_t stream) {
+  const Trace trace_("h3_qkv_proj");
   if (L < 1 || !valid_d(d)) return H3_ERR_INVALID_ARG;
   if (!aligned16(y) || !aligned16(Wqkv) || !aligned16(qkv)) return H3_ERR_INVALID_ARG;
   if (overlap(y, size_t(L) * d * 2, qkv, size_t(L) * 3 * d * 2)) return H3_ERR_INVALID_ARG;
@@ -164,11 +210,13 @@ h3_status h3_qkv_proj(const uint16_t* y, const uint16_t* Wqkv, int32_t L, int32_
   a.N = 3 * d;
   a.K = d;
   a.epilogue = EPI_PLAIN;
-  return launched(launch_gemm(a, ctx, reinterpret_cast<cudaStream_t>(stream)));
+  return finish(launched(launch_gemm(a, ctx, reinterpret_cast<cudaStream_t>(stream))),
+                stream);
 }
 
 h3_status h3_mrope_apply(uint16_t* qkv, const int32_t* pos, int32_t L, int32_t n_heads,
                          int32_t head_dim, const int32_t sec[3], float base, h3_stream_t stream) {
+  const Trace trace_("h3_mrope_apply");
   if (L < 1 || n_heads < 1) return H3_ERR_INVALID_ARG;
   if (head_dim != 128) return H3_ERR_UNSUPPORTED;
   if (!valid_d(n_heads * 128)) return H3_ERR_INVALID_ARG;
@@ -179,12 +227,15 @@ h3_status h3_mrope_apply(uint16_t* qkv, const int32_t* pos, int32_t L, int32_t n
   if (h3_status s = dev_ctx(&ctx)) return s;
   RopeTable rt;
   make_rope_table(&rt, sec, base);
-  return launched(launch_mrope(qkv, pos, L, n_heads, rt, ctx, reinterpret_cast<cudaStream_t>(stream)));
+  return finish(launched(launch_mrope(qkv, pos, L, n_heads, rt, ctx,
+                                      reinterpret_cast<cudaStream_t>(stream))),
+                stream);
 }
 
 h3_status h3_joint_attn_fwd(const uint16_t* qkv, int32_t L, int32_t n_heads, int32_t head_dim,
                             int32_t causal, float sm_scale, uint16_t* O, float* lse,
                             h3_stream_t stream) {
+  const Trace trace_("h3_joint_attn_fwd");
   if (L < 1 || n_heads < 1) return H3_ERR_INVALID_ARG;
   if (head_dim != 128) return H3_ERR_UNSUPPORTED;
   if (!valid_d(n_heads * 128)) return H3_ERR_INVALID_ARG;
@@ -204,13 +255,15 @@ h3_status h3_joint_attn_fwd(const uint16_t* qkv, int32_t L, int32_t n_heads, int
   a.H = n_heads;
   a.causal = causal;
   a.sm_scale = sm_scale;
-  return launched(launch_attention(a, ctx, reinterpret_cast<cudaStream_t>(stream)));
+  return finish(launched(launch_attention(a, ctx, reinterpret_cast<cudaStream_t>(stream))),
+                stream);
 }
 
 h3_status h3_joint_attn_varlen_fwd(const uint16_t* qkv, const int32_t* cu_seqlens,
                                    int32_t n_seg, int32_t L, int32_t n_heads, int32_t head_dim,
                                    int32_t causal, float sm_scale, uint16_t* O, float* lse,
                                    h3_stream_t stream) {
+  const Trace trace_("h3_joint_attn_varlen_fwd");
   if (L < 1 || n_heads < 1) return H3_ERR_INVALID_ARG;
   if (head_dim != 128) return H3_ERR_UNSUPPORTED;
   if (!valid_d(n_heads * 128)) return H3_ERR_INVALID_ARG;
@@ -233,7 +286,8 @@ h3_status h3_joint_attn_varlen_fwd(const uint16_t* qkv, const int32_t* cu_seqlen
   a.sm_scale = sm_scale;
   a.n_seg = n_seg;
   a.cu_seqlens = cu_seqlens;
-  return launched(launch_attention(a, ctx, reinterpret_cast<cudaStream_t>(stream)));
+  return finish(launched(launch_attention(a, ctx, reinterpret_cast<cudaStream_t>(stream))),
+                stream);
 }
 
 // Workspace of the fp8-score attention: qk8 [L][2d] bytes | sq [H][L] | sk [H][nkb].
@@ -253,6 +307,7 @@ h3_status h3_attn_workspace_size_fp8(int32_t L, int32_t n_heads, int32_t head_di
 
 h3_status h3_quantize_qk_fp8(const uint16_t* qkv, int32_t L, int32_t n_heads, int32_t head_dim,
                              uint8_t* qk8, float* sq, float* sk, h3_stream_t stream) {
+  const Trace trace_("h3_quantize_qk_fp8");
   if (L < 1 || n_heads < 1) return H3_ERR_INVALID_ARG;
   if (head_dim != 128) return H3_ERR_UNSUPPORTED;
   if (!valid_d(n_heads * 128)) return H3_ERR_INVALID_ARG;
@@ -267,14 +322,15 @@ h3_status h3_quantize_qk_fp8(const uint16_t* qkv, int32_t L, int32_t n_heads, in
     return H3_ERR_INVALID_ARG;
   DevCtx ctx;
   if (h3_status s = dev_ctx(&ctx)) return s;
-  return launched(launch_quantize_qk(qkv, L, n_heads, qk8, sq, sk, ctx,
-                                     reinterpret_cast<cudaStream_t>(stream)));
+  return finish(launched(launch_quantize_qk(qkv, L, n_heads, qk8, sq, sk, ctx,
+                                     reinterpret_cast<cudaStream_t>(stream))), stream);
 }
 
 h3_status h3_joint_attn_fwd_fp8(const uint16_t* qkv, int32_t L, int32_t n_heads,
                                 int32_t head_dim, int32_t causal, float sm_scale,
                                 void* workspace, size_t workspace_bytes, uint16_t* O, float* lse,
                                 h3_stream_t stream) {
+  const Trace trace_("h3_joint_attn_fwd_fp8");
   if (L < 1 || n_heads < 1) return H3_ERR_INVALID_ARG;
   if (head_dim != 128) return H3_ERR_UNSUPPORTED;
   if (!valid_d(n_heads * 128)) return H3_ERR_INVALID_ARG;
@@ -312,13 +368,14 @@ h3_status h3_joint_attn_fwd_fp8(const uint16_t* qkv, int32_t L, int32_t n_heads,
   a.qk8 = qk8;
   a.sq = sq;
   a.sk = sk;
-  return launched(launch_attention(a, ctx, st));
+  return finish(launched(launch_attention(a, ctx, st)), stream);
 }
 
 h3_status h3_out_proj_gated_residual(const uint16_t* O, const uint16_t* Wo,
                                      const uint16_t* x_res, const uint8_t* mod,
                                      const float* gate, int32_t L, int32_t d, int32_t n_mod,
                                      uint16_t* out, h3_stream_t stream) {
+  const Trace trace_("h3_out_proj_gated_residual");
   if (L < 1 || !valid_d(d) || n_mod < 1 || n_mod > 255) return H3_ERR_INVALID_ARG;
   if (!aligned16(O) || !aligned16(Wo) || !aligned16(x_res) || mod == nullptr ||
       !aligned16(gate) || !aligned16(out))
@@ -340,13 +397,15 @@ h3_status h3_out_proj_gated_residual(const uint16_t* O, const uint16_t* Wo,
   a.mod = mod;
   a.gate = gate;
   a.n_mod = n_mod;
-  return launched(launch_gemm(a, ctx, reinterpret_cast<cudaStream_t>(stream)));
+  return finish(launched(launch_gemm(a, ctx, reinterpret_cast<cudaStream_t>(stream))),
+                stream);
 }
 
 h3_status h3_denoise_step(float* z, float* x0, const uint16_t* v_h3, const uint8_t* mod,
                           const uint8_t* anchor, const float* z_anchor, int32_t L, int32_t C,
                           int32_t n_mod, const float* sigma, const float* sigma_next,
                           const uint8_t* update, h3_stream_t stream) {
+  const Trace trace_("h3_denoise_step");
   if (L < 1 || C < 4 || C % 4 != 0 || n_mod < 1 || n_mod > 255) return H3_ERR_INVALID_ARG;
   if (!aligned16(z) || !aligned16(v_h3) || mod == nullptr) return H3_ERR_INVALID_ARG;
   if (x0 != nullptr && !aligned16(x0)) return H3_ERR_INVALID_ARG;
@@ -364,8 +423,8 @@ h3_status h3_denoise_step(float* z, float* x0, const uint16_t* v_h3, const uint8
   }
   DevCtx ctx;
   if (h3_status s = dev_ctx(&ctx)) return s;
-  return launched(launch_denoise(z, x0, v_h3, mod, anchor, z_anchor, L, C, n_mod, dp, ctx,
-                                 reinterpret_cast<cudaStream_t>(stream)));
+  return finish(launched(launch_denoise(z, x0, v_h3, mod, anchor, z_anchor, L, C, n_mod, dp, ctx,
+                                 reinterpret_cast<cudaStream_t>(stream))), stream);
 }
 
 static h3_status check_mlp(const h3_mlp_desc* desc) {
@@ -390,6 +449,7 @@ h3_status h3_mlp_block_fwd(const h3_mlp_desc* desc, const uint16_t* x, const uin
                            const float* shift, const float* scale, const float* gate,
                            const uint16_t* W1, const uint16_t* W2, void* workspace,
                            size_t workspace_bytes, uint16_t* out, h3_stream_t stream) {
+  const Trace trace_("h3_mlp_block_fwd");
   size_t need = 0;
   if (h3_status s = h3_mlp_workspace_size(desc, &need)) return s;
   if (!aligned16(x) || mod == nullptr || !aligned16(shift) || !aligned16(scale) ||
@@ -432,24 +492,26 @@ h3_status h3_mlp_block_fwd(const h3_mlp_desc* desc, const uint16_t* x, const uin
   down.gate = gate;
   down.n_mod = desc->n_mod;
   if (launch_gemm(down, ctx, st) != cudaSuccess) return H3_ERR_CUDA;
-  return H3_OK;
+  return finish(H3_OK, stream);
 }
 
 h3_status h3_quantize_rows_fp8(const uint16_t* x, int32_t R, int32_t K, uint8_t* q, float* scale,
                                h3_stream_t stream) {
+  const Trace trace_("h3_quantize_rows_fp8");
   if (R < 1 || K < 16 || K % 16 != 0) return H3_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(q) || scale == nullptr ||
       (reinterpret_cast<uintptr_t>(scale) & 3u))
     return H3_ERR_INVALID_ARG;
   DevCtx ctx;
   if (h3_status s = dev_ctx(&ctx)) return s;
-  return launched(launch_quantize_rows(x, R, K, q, scale, ctx,
-                                       reinterpret_cast<cudaStream_t>(stream)));
+  return finish(launched(launch_quantize_rows(x, R, K, q, scale, ctx,
+                                       reinterpret_cast<cudaStream_t>(stream))), stream);
 }
 
 h3_status h3_gemm_fp8(const uint8_t* A, const float* a_scale, const uint8_t* B,
                       const float* b_scale, int32_t M, int32_t N, int32_t K, uint16_t* C,
                       h3_stream_t stream) {
+  const Trace trace_("h3_gemm_fp8");
   if (M < 1 || N < 128 || N % 128 != 0 || K < 128 || K % 128 != 0) return H3_ERR_INVALID_ARG;
   if (!aligned16(A) || !aligned16(B) || !aligned16(C) || !aligned16(a_scale) ||
       !aligned16(b_scale))
@@ -467,7 +529,8 @@ h3_status h3_gemm_fp8(const uint8_t* A, const float* a_scale, const uint8_t* B,
   g.fp8 = 1;
   g.a_scale = a_scale;
   g.b_scale = b_scale;
-  return launched(launch_gemm(g, ctx, reinterpret_cast<cudaStream_t>(stream)));
+  return finish(launched(launch_gemm(g, ctx, reinterpret_cast<cudaStream_t>(stream))),
+                stream);
 }
 
 static h3_status check_desc(const h3_block_desc* desc);
@@ -486,6 +549,7 @@ h3_status h3_attn_block_fwd_fp8(const h3_block_desc* desc, const uint16_t* x, co
                                 const float* gate, const uint8_t* Wqkv_q, const float* Wqkv_s,
                                 const uint8_t* Wo_q, const float* Wo_s, void* workspace,
                                 size_t workspace_bytes, uint16_t* out, h3_stream_t stream) {
+  const Trace trace_("h3_attn_block_fwd_fp8");
   size_t need = 0;
   if (h3_status s = h3_workspace_size_fp8(desc, &need)) return s;
   if (!aligned16(x) || mod == nullptr || pos == nullptr || (reinterpret_cast<uintptr_t>(pos) & 3u) ||
@@ -567,7 +631,7 @@ h3_status h3_attn_block_fwd_fp8(const h3_block_desc* desc, const uint16_t* x, co
   o.fp8 = 1;
   o.a_scale = s8;
   o.b_scale = Wo_s;
-  return launched(launch_gemm(o, ctx, st));
+  return finish(launched(launch_gemm(o, ctx, st)), stream);
 }
 
 static h3_status check_mlp(const h3_mlp_desc* desc);
@@ -585,6 +649,7 @@ h3_status h3_mlp_block_fwd_fp8(const h3_mlp_desc* desc, const uint16_t* x, const
                                const uint8_t* W1_q, const float* W1_s, const uint8_t* W2_q,
                                const float* W2_s, void* workspace, size_t workspace_bytes,
                                uint16_t* out, h3_stream_t stream) {
+  const Trace trace_("h3_mlp_block_fwd_fp8");
   size_t need = 0;
   if (h3_status s = h3_mlp_workspace_size_fp8(desc, &need)) return s;
   if (!aligned16(x) || mod == nullptr || !aligned16(shift) || !aligned16(scale) ||
@@ -638,7 +703,7 @@ h3_status h3_mlp_block_fwd_fp8(const h3_mlp_desc* desc, const uint16_t* x, const
   down.fp8 = 1;
   down.a_scale = s8;
   down.b_scale = W2_s;
-  return launched(launch_gemm(down, ctx, st));
+  return finish(launched(launch_gemm(down, ctx, st)), stream);
 }
 
 static h3_status check_desc(const h3_block_desc* desc) {
@@ -668,6 +733,7 @@ h3_status h3_attn_block_fwd(const h3_block_desc* desc, const uint16_t* x, const 
                             const float* gate, const uint16_t* Wqkv, const uint16_t* Wo,
                             void* workspace, size_t workspace_bytes, uint16_t* out,
                             h3_stream_t stream) {
+  const Trace trace_("h3_attn_block_fwd");
   return h3_attn_block_fwd_profiled(desc, x, mod, pos, shift, scale, gate, Wqkv, Wo, workspace,
                                     workspace_bytes, out, stream, nullptr);
 }
@@ -677,6 +743,7 @@ h3_status h3_attn_block_fwd_profiled(const h3_block_desc* desc, const uint16_t* 
                                      const float* scale, const float* gate, const uint16_t* Wqkv,
                                      const uint16_t* Wo, void* workspace, size_t workspace_bytes,
                                      uint16_t* out, h3_stream_t stream, void* const* events) {
+  const Trace trace_("h3_attn_block_fwd_profiled");
   size_t need = 0;
   if (h3_status s = h3_workspace_size(desc, &need)) return s;
   if (!aligned16(x) || mod == nullptr || pos == nullptr || (reinterpret_cast<uintptr_t>(pos) & 3u) ||
@@ -747,7 +814,7 @@ h3_status h3_attn_block_fwd_profiled(const h3_block_desc* desc, const uint16_t* 
   o.gate = gate;
   o.n_mod = desc->n_mod;
   if (launch_gemm(o, ctx, st) != cudaSuccess || !mark(4)) return H3_ERR_CUDA;
-  return H3_OK;
+  return finish(H3_OK, stream);
 }
 
 h3_status h3_sync_status(h3_stream_t stream) {
@@ -768,11 +835,13 @@ h3_status h3_sync_status(h3_stream_t stream) {
 }
 
 h3_status h3_selftest_wait_timeout(uint64_t limit_ns, h3_stream_t stream) {
+  const Trace trace_("h3_selftest_wait_timeout");
   if (limit_ns == 0 || limit_ns > 10000000000ull) return H3_ERR_INVALID_ARG;
   DevCtx ctx;
   if (h3_status s = dev_ctx(&ctx)) return s;
   ctx.wait_ns = limit_ns;
-  return launched(launch_wait_selftest(ctx, reinterpret_cast<cudaStream_t>(stream)));
+  return finish(launched(launch_wait_selftest(ctx, reinterpret_cast<cudaStream_t>(stream))),
+                stream);
 }
 
 }  // extern "C"

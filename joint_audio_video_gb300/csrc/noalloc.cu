@@ -6,14 +6,17 @@
 // executes, and a process whose caching allocator has already reserved the
 // GPU's memory may see a fresh cudaMalloc fail.  For them this entry point
 // uses a workspace that the library itself holds: a fixed-size array in
-// device global memory, created when the library's module is loaded on a GPU
-// and kept until the process exits.
+// device global memory, reserved when the library's module is loaded on a GPU
+// (with CUDA's lazy module loading, at the first lookup below) and kept until
+// the process exits.
 //
 // Host code cannot use the array's name as a device address (in host code the
 // symbol is only a host-side stand-in), so the device address is looked up
 // with cudaGetSymbolAddress once per device, with that device current, the
-// first time this entry point is called on it; make that first call before
-// any stream capture begins.  All calls on a device share the one array and
+// first time this entry point is called on it; make that first call during
+// set-up, before the caller's allocator takes the device's memory and before
+// any stream capture begins.  The address is kept for the life of the
+// process: a cudaDeviceReset() of the device is not supported.  All calls on a device share the one array and
 // the last call's contents stay in it; nothing in it needs to start at zero
 // (each stage writes its part before any stage reads it).  Calls whose work
 // overlaps on the GPU (different streams without ordering between them) race
