@@ -14,7 +14,8 @@
 //               (K_j, V_{j-1}) that block's products read (128 x 128 bf16 tiles,
 //               two 64-column boxes with 128-byte swizzle) under one barrier,
 //               into two pair slots
-//   warp 1      TMEM owner + single-thread tcgen05.mma issuer
+//   warp 1      TMEM owner + tcgen05.mma issuer (the warp runs the loop, one
+//               elected lane issues)
 //   warps 2..5  softmax warpgroup of tile 0 (one query row per thread)
 //   warps 6..9  softmax warpgroup of tile 1
 // Tensor memory (512 columns): S0 | S1 | O0 | O1, 128 fp32 columns each.  The
@@ -105,39 +106,6 @@ __device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
-#define H3_F(x) __uint_as_float(x)
-// Maximum of the 128 raw scores of a row as 8 interleaved chains of 8
-// three-input max operations (short dependency chains), then a 3-level tree.
-__device__ __forceinline__ float max128(const uint32_t (&r0)[32], const uint32_t (&r1)[32],
-                                       const uint32_t (&r2)[32], const uint32_t (&r3)[32]) {
-  float m[8];
-#pragma unroll
-  for (int q = 0; q < 2; ++q) {
-    m[0 + q] = max3(H3_F(r0[16 * q]), H3_F(r0[16 * q + 1]), H3_F(r0[16 * q + 2]));
-    m[2 + q] = max3(H3_F(r1[16 * q]), H3_F(r1[16 * q + 1]), H3_F(r1[16 * q + 2]));
-    m[4 + q] = max3(H3_F(r2[16 * q]), H3_F(r2[16 * q + 1]), H3_F(r2[16 * q + 2]));
-    m[6 + q] = max3(H3_F(r3[16 * q]), H3_F(r3[16 * q + 1]), H3_F(r3[16 * q + 2]));
-  }
-#pragma unroll
-  for (int i = 3; i < 15; i += 2) {
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      m[0 + q] = max3(m[0 + q], H3_F(r0[16 * q + i]), H3_F(r0[16 * q + i + 1]));
-      m[2 + q] = max3(m[2 + q], H3_F(r1[16 * q + i]), H3_F(r1[16 * q + i + 1]));
-      m[4 + q] = max3(m[4 + q], H3_F(r2[16 * q + i]), H3_F(r2[16 * q + i + 1]));
-      m[6 + q] = max3(m[6 + q], H3_F(r3[16 * q + i]), H3_F(r3[16 * q + i + 1]));
-    }
-  }
-#pragma unroll
-  for (int q = 0; q < 2; ++q) {
-    m[0 + q] = fmaxf(m[0 + q], H3_F(r0[16 * q + 15]));
-    m[2 + q] = fmaxf(m[2 + q], H3_F(r1[16 * q + 15]));
-    m[4 + q] = fmaxf(m[4 + q], H3_F(r2[16 * q + 15]));
-    m[6 + q] = fmaxf(m[6 + q], H3_F(r3[16 * q + 15]));
-  }
-  return fmaxf(max3(m[0], m[1], m[2]), max3(m[3], m[4], max3(m[5], m[6], m[7])));
-}
-#undef H3_F
 // p = 2^(s*c - m) for 32 raw scores: 16 bf16 pairs into pk, row sum into acc.
 __device__ __forceinline__ void exp32(const uint32_t (&r)[32], uint64_t cc, uint64_t nm,
                                       uint32_t* pk, uint64_t (&acc)[2]) {
@@ -150,6 +118,45 @@ __device__ __forceinline__ void exp32(const uint32_t (&r)[32], uint64_t cc, uint
     acc[i & 1] = fadd2(acc[i & 1], f2(a, b));
     pk[i] = pack_bf16x2(a, b);
   }
+}
+
+// exp32, plus the maximum of the 32 raw scores folded into two running chains
+// (for the pass that computes the exponentials before the block maximum is known).
+__device__ __forceinline__ void exp32_max(const uint32_t (&r)[32], uint64_t cc, uint64_t nm,
+                                          uint32_t* pk, uint64_t (&acc)[2], float (&mc)[2]) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const float s0 = __uint_as_float(r[2 * i]), s1 = __uint_as_float(r[2 * i + 1]);
+    mc[i & 1] = max3(mc[i & 1], s0, s1);
+    float a, b;
+    unf2(ffma2(f2(s0, s1), cc, nm), a, b);
+    a = ex2(a);
+    b = ex2(b);
+    acc[i & 1] = fadd2(acc[i & 1], f2(a, b));
+    pk[i] = pack_bf16x2(a, b);
+  }
+}
+
+// O (this thread's row, 128 fp32 columns in TMEM) times f.
+__device__ __forceinline__ void rescale_o(uint32_t tO, float f) {
+#pragma unroll 1
+  for (int c = 0; c < 4; ++c) {
+    uint32_t o[32];
+    tmem_ld32(tO + c * 32, o);
+    tmem_ld_wait(o);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
+    tmem_st32(tO + c * 32, o);
+  }
+  tmem_st_wait();
+}
+
+// Keys of block column c visible to the row iff lo_rel <= c < hi_rel.
+__device__ __forceinline__ void mask32(uint32_t (&r)[32], int base, int lo_rel, int hi_rel) {
+  constexpr uint32_t kNegInf = 0xFF800000u;
+#pragma unroll
+  for (int c = 0; c < 32; ++c)
+    if (c + base < lo_rel || c + base >= hi_rel) r[c] = kNegInf;
 }
 
 // The MMA issuer keeps every operand descriptor precomputed: issuing one
@@ -301,70 +308,87 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane_id() == 0) {
-      bool ok = mbar_wait(smem_u32(&bar_q), 0, wc);
-      // descriptors of Q0, Q1 and of every ring slot read as K (K-major) or V (MN-major)
-      const SDesc dQ0 = sdesc_split(sdesc_sw128(sQ, 16, 1024));
-      const SDesc dQ1 = sdesc_split(sdesc_sw128(sQ + kTile, 16, 1024));
-      // pair slots are 2 kTile apart, V one kTile after K: a descriptor is the
-      // first slot's plus the byte offset / 16
-      const SDesc dK0 = sdesc_split(sdesc_sw128(sRing, 16, 1024));
-      const SDesc dV0 = sdesc_split(sdesc_sw128(sRing + kTile, kBox, 1024));
-      auto dK = [&](int j) { return SDesc{dK0.lo + uint32_t(j & 1) * (2 * kTile >> 4), dK0.hi}; };
-      auto dV = [&](int j) { return SDesc{dV0.lo + uint32_t(j & 1) * (2 * kTile >> 4), dV0.hi}; };
-      auto pair_full = [&](int j) { return smem_u32(&bar_kv_full[j & 1]); };
-      auto pair_empty = [&](int j) { return smem_u32(&bar_kv_empty[j & 1]); };
-      const uint32_t tS0 = tmem, tS1 = tmem + 128, tO0 = tmem + 256, tO1 = tmem + 384;
-      if (ok) ok = mbar_wait(pair_full(0), 0, wc);
-      if (ok) {
-        tc_fence_after();
+    // The whole warp runs the loop (waits and descriptor arithmetic stay
+    // warp-uniform); one elected lane issues the products and commits.
+    const bool leader = elect_one();
+    auto wait_all = [&](uint32_t bar, uint32_t parity) {
+      return __all_sync(0xffffffffu, mbar_wait(bar, parity, wc));
+    };
+    bool ok = wait_all(smem_u32(&bar_q), 0);
+    // descriptors of Q0, Q1 and of every ring slot read as K (K-major) or V (MN-major)
+    const SDesc dQ0 = sdesc_split(sdesc_sw128(sQ, 16, 1024));
+    const SDesc dQ1 = sdesc_split(sdesc_sw128(sQ + kTile, 16, 1024));
+    // pair slots are 2 kTile apart, V one kTile after K: a descriptor is the
+    // first slot's plus the byte offset / 16
+    const SDesc dK0 = sdesc_split(sdesc_sw128(sRing, 16, 1024));
+    const SDesc dV0 = sdesc_split(sdesc_sw128(sRing + kTile, kBox, 1024));
+    auto dK = [&](int j) { return SDesc{dK0.lo + uint32_t(j & 1) * (2 * kTile >> 4), dK0.hi}; };
+    auto dV = [&](int j) { return SDesc{dV0.lo + uint32_t(j & 1) * (2 * kTile >> 4), dV0.hi}; };
+    auto pair_full = [&](int j) { return smem_u32(&bar_kv_full[j & 1]); };
+    auto pair_empty = [&](int j) { return smem_u32(&bar_kv_empty[j & 1]); };
+    const uint32_t tS0 = tmem, tS1 = tmem + 128, tO0 = tmem + 256, tO1 = tmem + 384;
+    if (ok) ok = wait_all(pair_full(0), 0);
+    if (ok) {
+      tc_fence_after();
+      if (leader) {
         s_product<FP8>(tS0, dQ0, dK(0));
         tc_commit(smem_u32(&bar_s[0]));
         s_product<FP8>(tS1, dQ1, dK(0));
         tc_commit(smem_u32(&bar_s[1]));
         tc_commit(pair_empty(0));
       }
-      // block j: P(j-1).V_{j-1} and S(j) for each tile, both tiles from pair j
-      for (int j = 1; j < nblk && ok; ++j) {
-        const uint32_t pph = (j - 1) & 1;
-        ok = mbar_wait(pair_full(j), (j >> 1) & 1, wc) &&
-             mbar_wait(smem_u32(&bar_p[0]), pph, wc);
-        if (!ok) break;
-        tc_fence_after();
-        pv_product(tO0, tS0, dV(j), j > 1);
+      __syncwarp();
+    }
+    // block j: P(j-1).V_{j-1} and S(j) for each tile, both tiles from pair j
+    for (int j = 1; j < nblk && ok; ++j) {
+      const uint32_t pph = (j - 1) & 1;
+      ok = wait_all(pair_full(j), (j >> 1) & 1) && wait_all(smem_u32(&bar_p[0]), pph);
+      if (!ok) break;
+      tc_fence_after();
+      if (leader) {
+        pv_product(tO0, tS0 + 64, dV(j), j > 1);
         s_product<FP8>(tS0, dQ0, dK(j));
         tc_commit(smem_u32(&bar_s[0]));
-        ok = mbar_wait(smem_u32(&bar_p[1]), pph, wc);
-        if (!ok) break;
-        tc_fence_after();
-        pv_product(tO1, tS1, dV(j), j > 1);
+      }
+      __syncwarp();
+      ok = wait_all(smem_u32(&bar_p[1]), pph);
+      if (!ok) break;
+      tc_fence_after();
+      if (leader) {
+        pv_product(tO1, tS1 + 64, dV(j), j > 1);
         s_product<FP8>(tS1, dQ1, dK(j));
         tc_commit(smem_u32(&bar_s[1]));
         tc_commit(pair_empty(j));
       }
+      __syncwarp();
+    }
+    if (ok) {
+      const int j = nblk;
+      const uint32_t pph = (j - 1) & 1;
+      ok = wait_all(pair_full(j), (j >> 1) & 1) && wait_all(smem_u32(&bar_p[0]), pph);
       if (ok) {
-        const int j = nblk;
-        const uint32_t pph = (j - 1) & 1;
-        ok = mbar_wait(pair_full(j), (j >> 1) & 1, wc) &&
-             mbar_wait(smem_u32(&bar_p[0]), pph, wc);
-        if (ok) {
-          tc_fence_after();
-          pv_product(tO0, tS0, dV(j), j > 1);
-          ok = mbar_wait(smem_u32(&bar_p[1]), pph, wc);
-        }
-        if (ok) {
-          tc_fence_after();
-          pv_product(tO1, tS1, dV(j), j > 1);
+        tc_fence_after();
+        if (leader) pv_product(tO0, tS0 + 64, dV(j), j > 1);
+        __syncwarp();
+        ok = wait_all(smem_u32(&bar_p[1]), pph);
+      }
+      if (ok) {
+        tc_fence_after();
+        if (leader) {
+          pv_product(tO1, tS1 + 64, dV(j), j > 1);
           tc_commit(pair_empty(j));
           tc_commit(smem_u32(&bar_o));
         }
+        __syncwarp();
       }
-      tc_commit(smem_u32(&bar_drain));
-      WaitCtx drain{&abort_flag, p.status, kDrainWaitNs};
-      volatile int no_abort = 0;
-      drain.abort = &no_abort;
-      mbar_wait(smem_u32(&bar_drain), 0, drain);
     }
+    // let every product issued so far finish before the CTA frees tensor memory
+    if (leader) tc_commit(smem_u32(&bar_drain));
+    __syncwarp();
+    WaitCtx drain{&abort_flag, p.status, kDrainWaitNs};
+    volatile int no_abort = 0;
+    drain.abort = &no_abort;
+    mbar_wait(smem_u32(&bar_drain), 0, drain);
   } else {
     // ------------------------------------------------------------ softmax
     const int g = (warp - 2) >> 2;          // tile 0 or 1
@@ -407,51 +431,65 @@ __global__ void __launch_bounds__(kThreads, 1)
       // block columns c are keys kv_lo + 128 j + c; visible iff lo_rel <= c < hi_rel
       const int kv0 = kv_lo + j * 128;
       const int lo_rel = row_lo - kv0, hi_rel = row_hi - kv0;
-      if (__any_sync(0xffffffffu, lo_rel > 0 || hi_rel < 128)) {
-        constexpr uint32_t kNegInf = 0xFF800000u;
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          if (c < lo_rel || c >= hi_rel) r0[c] = kNegInf;
-          if (c + 32 < lo_rel || c + 32 >= hi_rel) r1[c] = kNegInf;
-          if (c + 64 < lo_rel || c + 64 >= hi_rel) r2[c] = kNegInf;
-          if (c + 96 < lo_rel || c + 96 >= hi_rel) r3[c] = kNegInf;
-        }
+      const bool masked = __any_sync(0xffffffffu, lo_rel > 0 || hi_rel < 128);
+      if (masked) {
+        mask32(r0, 0, lo_rel, hi_rel);
+        mask32(r1, 32, lo_rel, hi_rel);
+        mask32(r2, 64, lo_rel, hi_rel);
+        mask32(r3, 96, lo_rel, hi_rel);
       }
-      // row maximum of the raw scores (scale > 0 commutes with max); -inf while
-      // no key of this row has been seen, and then O and l hold only zeros
-      const float mx = max128(r0, r1, r2, r3) * c;
-      {
-        const float m_new = fmaxf(m_used, mx);
-        const bool fresh = m_used == -INFINITY;
-        const bool need = !fresh && m_new > m_used + kRescaleThreshold;
-        if (fresh) m_used = m_new;
-        if (__any_sync(0xffffffffu, need)) {
-          const float f = need ? ex2(m_used - m_new) : 1.f;
-#pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
-            uint32_t o[32];
-            tmem_ld32(tO + c * 32, o);
-            tmem_ld_wait(o);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
-            tmem_st32(tO + c * 32, o);
-          }
-          tmem_st_wait();
-          l *= f;
-          if (need) m_used = m_new;
-        }
-      }
-      // p = 2^(s * scale_log2 - m_used), rounded to bf16 pairs over S's first 64 columns
-      const float neg_m = m_used == -INFINITY ? 0.f : -m_used;   // all scores -inf: p = 0
-      const uint64_t cc = f2(c, c), nm = f2(neg_m, neg_m);
+      // P (bf16 pairs) goes over the second half of S (columns 64..127): the
+      // first half keeps the raw scores of keys 0..63 for an exact redo, and
+      // the scores of keys 64..127 are still in r2, r3 when P overwrites them
+      // p = 2^(s * c - m_used) straight away, with the block maximum taken in
+      // the same pass.  Only when that maximum exceeds the running one by more
+      // than the threshold is the block redone against the new maximum: rare
+      // once a row has seen a few blocks, and always for a row's first visible
+      // block (no running maximum yet: the pass runs against 0 and is discarded).
       uint64_t acc[2] = {0ull, 0ull};
       uint32_t pk0[32], pk1[32];
-      exp32(r0, cc, nm, pk0, acc);
-      exp32(r1, cc, nm, pk0 + 16, acc);
-      tmem_st32(tS, pk0);
-      exp32(r2, cc, nm, pk1, acc);
-      exp32(r3, cc, nm, pk1 + 16, acc);
-      tmem_st32(tS + 32, pk1);
+      const uint64_t cc = f2(c, c);
+      float neg_m = m_used == -INFINITY ? 0.f : -m_used;
+      uint64_t nm = f2(neg_m, neg_m);
+      float mc[2] = {-INFINITY, -INFINITY};
+      exp32_max(r0, cc, nm, pk0, acc, mc);
+      exp32_max(r1, cc, nm, pk0 + 16, acc, mc);
+      tmem_st32(tS + 64, pk0);
+      exp32_max(r2, cc, nm, pk1, acc, mc);
+      exp32_max(r3, cc, nm, pk1 + 16, acc, mc);
+      tmem_st32(tS + 96, pk1);
+      // raw maximum times c (> 0); -inf while no key of the row is visible
+      const float mx = fmaxf(mc[0], mc[1]) * c;
+      const bool need = mx > m_used + kRescaleThreshold;   // -inf + 8 = -inf: a first key
+      if (__any_sync(0xffffffffu, need)) {
+        // O and l hold the blocks before this one against m_used; nothing yet
+        // for a row without a running maximum (f = 0 keeps them at zero)
+        const float m_new = need ? mx : m_used;
+        const float f = need ? (m_used == -INFINITY ? 0.f : ex2(m_used - m_new)) : 1.f;
+        rescale_o(tO, f);
+        l *= f;
+        m_used = m_new;
+        // the speculative P stores land before their replacements; keys 0..63
+        // come back from the first half of S, keys 64..127 are still in r2, r3
+        tmem_st_wait();
+        tmem_ld32(tS, r0);
+        tmem_ld32(tS + 32, r1);
+        tmem_ld_wait(r0);
+        tmem_ld_wait(r1);
+        if (masked) {
+          mask32(r0, 0, lo_rel, hi_rel);
+          mask32(r1, 32, lo_rel, hi_rel);
+        }
+        neg_m = m_used == -INFINITY ? 0.f : -m_used;
+        nm = f2(neg_m, neg_m);
+        acc[0] = acc[1] = 0ull;
+        exp32(r0, cc, nm, pk0, acc);
+        exp32(r1, cc, nm, pk0 + 16, acc);
+        tmem_st32(tS + 64, pk0);
+        exp32(r2, cc, nm, pk1, acc);
+        exp32(r3, cc, nm, pk1 + 16, acc);
+        tmem_st32(tS + 96, pk1);
+      }
       float a0, a1, b0, b1;
       unf2(acc[0], a0, a1);
       unf2(acc[1], b0, b1);

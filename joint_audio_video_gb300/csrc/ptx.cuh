@@ -29,6 +29,14 @@ __device__ __forceinline__ uint64_t global_ns() {
 }
 
 __device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31u; }
+// One lane of the (fully active) warp, the same on every call.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t e;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(e));
+  return e != 0;
+}
 __device__ __forceinline__ uint32_t warp_id() { return threadIdx.x >> 5; }
 
 // ------------------------------------------------------------------ mbarrier
