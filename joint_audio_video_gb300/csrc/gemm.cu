@@ -14,7 +14,8 @@
 // Layout of the work (one CTA per SM, 192 threads):
 //   warp 0      TMA producer: A tile 128x64 and B tile BNx64 per k-block into a
 //               4-stage shared-memory ring (128-byte swizzle, 1 KB aligned)
-//   warp 1      TMEM allocation + one elected thread issuing tcgen05.mma
+//   warp 1      TMEM allocation + tcgen05.mma issue (the warp runs the loop,
+//               one elected lane issues)
 //               (M=128, N=BN, K=16 per instruction) into one of two TMEM
 //               accumulators (2 x BN fp32 columns)
 //   warps 2..5  epilogue: tcgen05.ld of one accumulator row per thread, fused
@@ -258,26 +259,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
-    if (lane_id() == 0) {
-      constexpr uint32_t idesc = FP8 ? idesc_e4m3_f32(BM, BN) : idesc_bf16_f32(BM, BN, 0, 0);
-      // stages are kStageBytes apart: precomputed descriptors plus one add per MMA
-      const SDesc dA0 = sdesc_split(sdesc_sw128(base, 16, 1024));
-      const SDesc dB0 = sdesc_split(sdesc_sw128(base + Cfg::kABytes, 16, 1024));
-      int stage = 0;
-      uint32_t phase = 0;
-      int it = 0;
-      bool ok = true;
-      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++it) {
-        const int acc = it & 1;
-        const uint32_t acc_phase = (it >> 1) & 1;
-        if (!mbar_wait(smem_u32(&bar_acc_empty[acc]), acc_phase ^ 1u, wc)) { ok = false; break; }
+    // The whole warp runs the loop (waits and descriptor arithmetic stay
+    // warp-uniform); one elected lane issues the products and commits.
+    const bool leader = elect_one();
+    constexpr uint32_t idesc = FP8 ? idesc_e4m3_f32(BM, BN) : idesc_bf16_f32(BM, BN, 0, 0);
+    // stages are kStageBytes apart: precomputed descriptors plus one add per MMA
+    const SDesc dA0 = sdesc_split(sdesc_sw128(base, 16, 1024));
+    const SDesc dB0 = sdesc_split(sdesc_sw128(base + Cfg::kABytes, 16, 1024));
+    int stage = 0;
+    uint32_t phase = 0;
+    int it = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++it) {
+      const int acc = it & 1;
+      const uint32_t acc_phase = (it >> 1) & 1;
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_acc_empty[acc]), acc_phase ^ 1u, wc));
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t dtm = tmem + acc * BN;
+      for (int kb = 0; kb < kblocks; ++kb) {
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_full[stage]), phase, wc));
+        if (!ok) break;
         tc_fence_after();
-        const uint32_t dtm = tmem + acc * BN;
-        for (int kb = 0; kb < kblocks; ++kb) {
-          if (!mbar_wait(smem_u32(&bar_full[stage]), phase, wc)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t soff = stage * (Cfg::kStageBytes >> 4);
-          const SDesc dA{dA0.lo + soff, dA0.hi}, dB{dB0.lo + soff, dB0.hi};
+        const uint32_t soff = stage * (Cfg::kStageBytes >> 4);
+        const SDesc dA{dA0.lo + soff, dA0.hi}, dB{dB0.lo + soff, dB0.hi};
+        if (leader) {
           // 4 steps of 32 bytes along K: K=16 for bf16, K=32 for fp8
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
@@ -287,18 +293,21 @@ __global__ void __launch_bounds__(kThreads, 1)
               mma_bf16_ss(dtm, sdesc_at(dA, k * 32), sdesc_at(dB, k * 32), idesc, (kb | k) != 0);
           }
           tc_commit(smem_u32(&bar_empty[stage]));
-          if (++stage == S) { stage = 0; phase ^= 1u; }
         }
-        if (!ok) break;
-        tc_commit(smem_u32(&bar_acc_full[acc]));
+        __syncwarp();
+        if (++stage == S) { stage = 0; phase ^= 1u; }
       }
-      // drain: every MMA issued so far has finished before TMEM is released
-      tc_commit(smem_u32(&bar_drain));
-      WaitCtx drain{&abort_flag, p.status, kDrainWaitNs};
-      volatile int no_abort = 0;
-      drain.abort = &no_abort;
-      mbar_wait(smem_u32(&bar_drain), 0, drain);
+      if (!ok) break;
+      if (leader) tc_commit(smem_u32(&bar_acc_full[acc]));
+      __syncwarp();
     }
+    // drain: every MMA issued so far has finished before TMEM is released
+    if (leader) tc_commit(smem_u32(&bar_drain));
+    __syncwarp();
+    WaitCtx drain{&abort_flag, p.status, kDrainWaitNs};
+    volatile int no_abort = 0;
+    drain.abort = &no_abort;
+    mbar_wait(smem_u32(&bar_drain), 0, drain);
   } else {
     // ---------------------------------------------------------------- epilogue
     const int q = warp & 3;                 // TMEM lane quarter of this warp
