@@ -86,36 +86,44 @@ def test_full_block_slice_rows(h3):
 
 
 # ---------------------------------------------------------------------------
-# The lazy rescale at full length.  The kernel moves a row's running maximum
-# (and rescales O and l in tensor memory) only when a key block's maximum
-# exceeds it by more than 8 in log2 units.  With unit-variance scores that
-# never happens after the first blocks, so two heads are planted: in head 0 a
-# group of query rows meets a ramp over the last 2,000 keys (the maximum moves
-# several times, late), in head 1 the same rows meet 6 large keys that sit in
-# the masked tail block alone (one jump, in the block that holds only 6 valid
-# keys).  Whether a row takes the path is worked out below from the inputs.
+# Moves of the running maximum at full length.  The kernel computes a block's
+# exponentials against the row's running maximum and redoes the block when
+# its maximum exceeds that by more than 8 (log2 units).  With unit-variance
+# scores that never happens after the first blocks, so four heads are
+# planted: in head 0 a group of query rows meets a ramp over the last 2,000
+# keys (the maximum moves several times, late), in head 1 the same rows meet
+# 6 large keys that sit in the masked tail block alone, and in heads 2 and 3
+# they meet one key ~100 log2 units above everything before it, in the first
+# and in the second half of a late block (the exponentials of the first pass
+# over such a block reach 2^100).  Whether a row takes each path is worked
+# out below from the inputs.
 # ---------------------------------------------------------------------------
 RESCALE_LOG2 = 8.0
+BIG_LOG2 = 64.0
+
+
+def _block_maxima(qkv64, H, rows, causal, sm_scale, h, width):
+    """Per row: maxima (log2 units) of consecutive key groups of `width`."""
+    L = qkv64.shape[0]
+    d = H * 128
+    q = qkv64[rows, h * 128:(h + 1) * 128]
+    k = qkv64[:, d + h * 128:d + (h + 1) * 128]
+    s = (q @ k.T) * (sm_scale / math.log(2.0))
+    if causal:
+        s = np.where(np.arange(L)[None, :] <= rows[:, None], s, -np.inf)
+    n = (L + width - 1) // width
+    pad = np.full((len(rows), n * width - L), -np.inf)
+    return np.concatenate([s, pad], axis=1).reshape(len(rows), n, width).max(axis=2)
 
 
 def _rescale_events(qkv64, H, rows, causal, sm_scale):
-    """Per (head, row): how many key blocks move the running maximum under the
-    kernel's rule (block maximum above the running one by more than 8 log2)."""
-    L = qkv64.shape[0]
-    d = H * 128
-    c = sm_scale / math.log(2.0)
+    """Per (head, row): how many key blocks move the running maximum by more
+    than 8 (log2 units) over the maximum of everything before them."""
     ev = np.zeros((H, len(rows)), dtype=np.int64)
-    nblk = (L + 127) // 128
     for h in range(H):
-        q = qkv64[rows, h * 128:(h + 1) * 128]
-        k = qkv64[:, d + h * 128:d + (h + 1) * 128]
-        s = (q @ k.T) * c
-        if causal:
-            s = np.where(np.arange(L)[None, :] <= rows[:, None], s, -np.inf)
-        pad = np.full((len(rows), nblk * 128 - L), -np.inf)
-        bm = np.concatenate([s, pad], axis=1).reshape(len(rows), nblk, 128).max(axis=2)
+        bm = _block_maxima(qkv64, H, rows, causal, sm_scale, h, 128)
         m = np.full(len(rows), -np.inf)
-        for b in range(nblk):
+        for b in range(bm.shape[1]):
             fresh = np.isinf(m)
             move = ~fresh & (bm[:, b] > m + RESCALE_LOG2)
             ev[h] += move
@@ -123,9 +131,20 @@ def _rescale_events(qkv64, H, rows, causal, sm_scale):
     return ev
 
 
+def _largest_jump(qkv64, H, rows, causal, sm_scale, h):
+    """Per row: the largest amount (log2 units) by which a 64-key half block
+    exceeds the maximum of all keys before it."""
+    hm = _block_maxima(qkv64, H, rows, causal, sm_scale, h, 64)
+    before = np.maximum.accumulate(np.concatenate(
+        [np.full((len(rows), 1), -np.inf), hm[:, :-1]], axis=1), axis=1)
+    with np.errstate(invalid="ignore"):
+        jump = np.where(np.isinf(before), -np.inf, hm - before)
+    return jump.max(axis=1)
+
+
 @pytest.mark.parametrize("causal", [False, True])
-def test_full_attention_lazy_rescale(h3, causal):
-    L, H = CONFIGS["full"].L, 2
+def test_full_attention_running_maximum_moves(h3, causal):
+    L, H = CONFIGS["full"].L, 4
     d = H * 128
     base = attention_qkv(L, H, seed=59).float()
     planted = random_rows(L, 160, seed=60).numpy()
@@ -138,19 +157,32 @@ def test_full_attention_lazy_rescale(h3, causal):
     # head 1: only the 6 keys of the last (ragged) block carry the large component
     base[L - 6:, d + 128:d + 136] += 6.0
     base[pin, 128:136] += 4.0
+    # heads 2 and 3: one key far above all others, in the first half (column 10)
+    # and in the second half (column 100) of the fifth block from the end
+    kb = ((L + 127) // 128 - 5) * 128
+    base[kb + 10, d + 256:d + 264] += 10.0
+    base[pin, 256:264] += 10.0
+    base[kb + 100, d + 384:d + 392] += 10.0
+    base[pin, 384:392] += 10.0
     qkv = base.to(torch.bfloat16)
     q64 = to64(qkv)
     sm = 1 / math.sqrt(128)
     ev = _rescale_events(q64, H, planted, causal, sm)
     late = planted >= L - 2000
     assert late.sum() >= 40
-    # the inputs really drive the rows through the path: several moves in head
-    # 0 for every planted row that sees the ramp, one in head 1 for every row
-    # that sees the tail block
+    # the inputs really drive the rows through each path: several moves in
+    # head 0 for every planted row that sees the ramp, one in head 1 for every
+    # row that sees the tail block, a jump above 64 in heads 2 and 3 for every
+    # row that sees the planted key
     seen0 = planted >= L - 1000 if causal else np.ones_like(late)
     assert np.all(ev[0][seen0] >= 2), ev[0][seen0].min()
     seen1 = planted >= L - 6 if causal else np.ones_like(late)
     assert np.all(ev[1][seen1] >= 1)
+    for h, col in ((2, kb + 10), (3, kb + 100)):
+        seen = planted >= col if causal else np.ones_like(late)
+        assert seen.sum() >= 40
+        jump = _largest_jump(q64, H, planted[seen], causal, sm, h)
+        assert np.all(jump > BIG_LOG2 + 8), jump.min()
     O = torch.full((L, d), float("nan"), dtype=torch.bfloat16, device=DEV)
     lse = torch.empty(H, L, dtype=torch.float32, device=DEV)
     h3.h3_joint_attn_fwd(qkv.to(DEV), L, H, 128, int(causal), sm, O, lse)
@@ -158,5 +190,5 @@ def test_full_attention_lazy_rescale(h3, causal):
     rows = np.unique(np.concatenate([planted, random_rows(L, 64, seed=61).numpy()]))
     ro, rl = orc.attention(q64, H, 128, causal=causal, sm_scale=sm, rows=rows)
     ridx = torch.from_numpy(rows).to(DEV)
-    assert_parity(to64(O[ridx]), ro, f"lazy-rescale rows (causal={causal})")
+    assert_parity(to64(O[ridx]), ro, f"running-maximum rows (causal={causal})")
     np.testing.assert_allclose(to64(lse[:, ridx]), rl, atol=2e-2, rtol=1e-3)
