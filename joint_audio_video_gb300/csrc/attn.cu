@@ -19,7 +19,7 @@
 //   warps 2..5  softmax warpgroup of tile 0 (one query row per thread)
 //   warps 6..9  softmax warpgroup of tile 1
 // Tensor memory (512 columns): S0 | S1 | O0 | O1, 128 fp32 columns each.  The
-// softmax writes P (bf16 pairs) over the first 64 columns of its S buffer and
+// softmax writes P (bf16 pairs) over the last 64 columns of its S buffer and
 // the P.V product reads it from TMEM as the A operand; V is the MN-major B
 // operand straight from the TMA tile.
 // MMA order per key block j:  P0V(j-1), S0(j), P1V(j-1), S1(j), so the tensor
