@@ -13,8 +13,11 @@
 // rate.  A row (d bf16) is read once from shared memory into registers (5
 // 16-byte vectors per thread at d = 5120); mean and variance are two exact
 // passes over the registers (fp32 warp shuffles + a shared-memory hop across
-// the 4 warps).  The per-modality fp32 vectors are tiny (n_mod x d) and served
-// from L1/L2.  Algorithmic traffic: 4*d bytes per row (read x, write y).
+// the 4 warps).  For d <= 6144, (1 + scale[m]) and shift[m] of the thread's
+// columns stay in registers and are reloaded (from L2: n_mod x d floats in
+// all) only when the modality changes from one row to the next; wider rows
+// read them per row through L1.  Algorithmic traffic: 4*d bytes
+// per row (read x, write y).
 #include <cuda_bf16.h>
 
 #include "kernels.hpp"

@@ -11,7 +11,9 @@
 //   EPI_GELU            C = gelu(acc), tanh form                    (feed-forward up
 //                       projection ff.net.0.proj of the MLP sub-block)
 //
-// Layout of the work (one CTA per SM, 192 threads):
+// Two forms.  For N % 256 == 0 a CTA pair (tcgen05 cta_group::2, clusters of
+// two) computes 256 x 256 tiles; see gemm_pair_kernel below.  Otherwise the
+// single-CTA form, laid out as follows (one CTA per SM, 192 threads):
 //   warp 0      TMA producer: A tile 128x64 and B tile BNx64 per k-block into a
 //               4-stage shared-memory ring (128-byte swizzle, 1 KB aligned)
 //   warp 1      TMEM allocation + tcgen05.mma issue (the warp runs the loop,
