@@ -8,22 +8,31 @@
 // keys >= L are masked here, nothing is padded); "多模态强化学习工程解析…",
 // 三 目标模型 (causal attention over the packed sequence, kept as an option).
 //
-// One CTA = one head x 256 query rows, as two 128-row tiles Q0, Q1 that share
-// every K/V block fetched.  320 threads:
+// One cluster of two CTAs (a CTA pair, tcgen05 cta_group::2) = one head x 512
+// query rows; each CTA holds 256 of them as two 128-row tiles Q0, Q1.  The
+// products of tile g are issued once for the pair (M = 256: the g-th tiles of
+// both CTAs) by the even CTA's MMA warp: S_g = Q_g K^T reads each CTA's Q_g
+// and the 64 keys of K that each CTA holds, P_g V reads each CTA's P_g from its
+// tensor memory and the 64 head dims of V that each CTA holds, and every
+// product writes 128 rows into the tensor memory of each CTA.  So each SM
+// loads half of every K/V block and issues half the products of a single-CTA
+// kernel.  320 threads per CTA:
 //   warp 0      TMA producer: Q0|Q1 once, then per key block j the pair
-//               (K_j, V_{j-1}) that block's products read (128 x 128 bf16 tiles,
-//               two 64-column boxes with 128-byte swizzle) under one barrier,
-//               into two pair slots
-//   warp 1      TMEM owner + tcgen05.mma issuer (the warp runs the loop, one
-//               elected lane issues)
+//               (K_j, V_{j-1}) that block's products read -- this CTA's 64 keys
+//               of K_j (two 64 x 64 boxes, 128-byte swizzle) and its 64 dims of
+//               V_{j-1} (one 128 x 64 box) -- into a ring of pair slots; the
+//               copies of both CTAs count on the even CTA's barrier
+//   warp 1      TMEM owner (both CTAs allocate together); in the even CTA the
+//               tcgen05.mma issuer (the warp runs the loop, one elected lane
+//               issues and commits to the barriers of both CTAs)
 //   warps 2..5  softmax warpgroup of tile 0 (one query row per thread)
 //   warps 6..9  softmax warpgroup of tile 1
-// Tensor memory (512 columns): S0 | S1 | O0 | O1, 128 fp32 columns each.  The
-// softmax writes P (bf16 pairs) over the last 64 columns of its S buffer and
-// the P.V product reads it from TMEM as the A operand; V is the MN-major B
-// operand straight from the TMA tile.
+// Tensor memory (512 columns per CTA): S0 | S1 | O0 | O1, 128 fp32 columns
+// each.  The softmax writes P (bf16 pairs) over the last 64 columns of its S
+// buffer and the P.V product reads it from TMEM as the A operand; V is the
+// MN-major B operand straight from the TMA tile.
 // MMA order per key block j:  P0V(j-1), S0(j), P1V(j-1), S1(j), so the tensor
-// core computes one tile's products while the other tile's softmax runs.
+// cores compute one tile's products while the other tile's softmax runs.
 // Softmax works in the log2 domain with a per-row running maximum that is
 // only moved (and O, l rescaled in TMEM) when the block maximum exceeds it by
 // more than 8 (factor 256): the final O / l is exact for any such maximum.
@@ -44,11 +53,13 @@ namespace h3 {
 namespace {
 
 constexpr int kThreads = 320;
-constexpr int kSlots = 2;    // K/V pair slots of two tiles each (K_j, V_{j-1})
+constexpr int kSlots = 4;                     // pair slots (K_j half | V_{j-1} half)
 constexpr uint32_t kTile = 128 * 128 * 2;     // one 128x128 bf16 tile (two 16 KB boxes)
-constexpr uint32_t kBox = 128 * 64 * 2;
+constexpr uint32_t kBox = 128 * 64 * 2;       // 128 rows x 64 bf16
+constexpr uint32_t kHalfBox = 64 * 64 * 2;    // 64 rows x 64 bf16
 constexpr uint32_t kTile8 = 128 * 128;        // one 128x128 E4M3 tile (one 16 KB box)
-constexpr size_t kSmem = 2 * kTile + 2 * kSlots * kTile + 1024;
+constexpr uint32_t kSlotBytes = 2 * kBox;     // this CTA's K half (16 KB) | V half (16 KB)
+constexpr size_t kSmem = 2 * kTile + kSlots * kSlotBytes + 1024;
 constexpr float kRescaleThreshold = 8.0f;     // log2 units
 
 struct AttnDev {
@@ -57,7 +68,7 @@ struct AttnDev {
   int L, H, d;
   int causal;
   float scale_log2;   // sm_scale * log2(e)
-  int num_pairs;
+  int num_quads;                  // clusters per head: 512 query rows each
   int* status;
   uint64_t wait_ns;
   int n_seg;                      // 0: one segment [0, L)
@@ -160,34 +171,35 @@ __device__ __forceinline__ void mask32(uint32_t (&r)[32], int base, int lo_rel, 
 }
 
 // The MMA issuer keeps every operand descriptor precomputed: issuing one
-// 128x128x16 MMA (64 tensor-core cycles) must cost far less than 64 cycles
-// of the issuing thread, or the tensor core waits on the issuer.
-// S = Q K^T: both K-major, 8 steps of K=16 over the two 64-column boxes.
+// 256x128x16 pair product (64 tensor-core cycles on each SM) must cost far
+// less than 64 cycles of the issuing thread, or the tensor cores wait on it.
+// S = Q K^T: both K-major, 8 steps of K=16 over the two 64-column boxes (each
+// CTA: Q boxes of 128 rows, K boxes of its 64 keys).
 template <bool FP8>
 __device__ __forceinline__ void s_product(uint32_t d_tmem, SDesc q, SDesc k) {
   if constexpr (FP8) {
     // E4M3: one 128-byte row holds the head's 128 dims; 4 steps of K = 32
-    constexpr uint32_t idesc = idesc_e4m3_f32(128, 128);
+    constexpr uint32_t idesc = idesc_e4m3_f32(256, 128);
 #pragma unroll
     for (int s = 0; s < 4; ++s)
-      mma_f8_ss(d_tmem, sdesc_at(q, s * 32), sdesc_at(k, s * 32), idesc, s > 0);
+      mma_f8_ss_pair(d_tmem, sdesc_at(q, s * 32), sdesc_at(k, s * 32), idesc, s > 0);
   } else {
-    constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 0, 0);
+    constexpr uint32_t idesc = idesc_bf16_f32(256, 128, 0, 0);
 #pragma unroll
-    for (int s = 0; s < 8; ++s) {
-      const uint32_t off = (s >> 2) * kBox + (s & 3) * 32;
-      mma_bf16_ss(d_tmem, sdesc_at(q, off), sdesc_at(k, off), idesc, s > 0);
-    }
+    for (int s = 0; s < 8; ++s)
+      mma_bf16_ss_pair(d_tmem, sdesc_at(q, (s >> 2) * kBox + (s & 3) * 32),
+                       sdesc_at(k, (s >> 2) * kHalfBox + (s & 3) * 32), idesc, s > 0);
   }
 }
 
-// O += P V: P (bf16 pairs) from TMEM, V as the MN-major operand, 8 steps of 16 keys.
+// O += P V: P (bf16 pairs) from TMEM, V as the MN-major operand (each CTA: its
+// 64 head dims), 8 steps of 16 keys.
 __device__ __forceinline__ void pv_product(uint32_t o_tmem, uint32_t p_tmem, SDesc v,
                                            bool accumulate) {
-  constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 0, 1);
+  constexpr uint32_t idesc = idesc_bf16_f32(256, 128, 0, 1);
 #pragma unroll
   for (int s = 0; s < 8; ++s)
-    mma_bf16_ts(o_tmem, p_tmem + s * 8, sdesc_at(v, s * 2048), idesc, accumulate || s > 0);
+    mma_bf16_ts_pair(o_tmem, p_tmem + s * 8, sdesc_at(v, s * 2048), idesc, accumulate || s > 0);
 }
 
 // Registers are split over the SM's four sub-partitions (16K each) and warp w
@@ -195,7 +207,8 @@ __device__ __forceinline__ void pv_product(uint32_t o_tmem, uint32_t p_tmem, SDe
 // at most 168 registers per thread.
 template <bool FP8>
 __global__ void __launch_bounds__(kThreads, 1)
-    attn_fwd_kernel(const __grid_constant__ CUtensorMap tm, const __grid_constant__ CUtensorMap tm8,
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tm, const __grid_constant__ CUtensorMap tmk,
+                    const __grid_constant__ CUtensorMap tm8, const __grid_constant__ CUtensorMap tm8k,
                     const __grid_constant__ AttnDev p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t bar_q, bar_kv_full[kSlots], bar_kv_empty[kSlots], bar_s[2], bar_p[2],
@@ -207,47 +220,53 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sQ = base;                 // Q0 at sQ, Q1 at sQ + kTile
   const uint32_t sRing = base + 2 * kTile;
   const int warp = warp_id();
+  const uint32_t rank = cluster_ctarank();  // 0: issues the pair's products
+  const bool lead = rank == 0;
   const WaitCtx wc{&abort_flag, p.status, p.wait_ns};
 
-  int pair = blockIdx.x % p.num_pairs;
-  const int h = blockIdx.x / p.num_pairs;
-  if (p.causal) pair = p.num_pairs - 1 - pair;   // longest rows first
-  const int q0 = pair * 256;
-  const int r_last = min(q0 + 255, p.L - 1);
-  // keys this CTA visits: the union of its rows' segments, cut at the diagonal
+  const int cl = blockIdx.x >> 1;
+  int quad = cl % p.num_quads;
+  const int h = cl / p.num_quads;
+  if (p.causal) quad = p.num_quads - 1 - quad;   // longest rows first
+  const int c0 = quad * 512;                     // the pair's rows: c0 .. c0 + 511
+  const int c_last = min(c0 + 511, p.L - 1);
+  const int q0 = c0 + int(rank) * 256;           // this CTA's rows: q0 .. q0 + 255
+  // keys the pair visits: the union of its rows' segments, cut at the diagonal
   int kv_lo = 0, kv_hi = p.L;
   if (p.n_seg > 0) {
-    kv_lo = p.cu[segment_of(p, q0)];
-    kv_hi = p.cu[segment_of(p, r_last) + 1];
+    kv_lo = p.cu[segment_of(p, c0)];
+    kv_hi = p.cu[segment_of(p, c_last) + 1];
   }
-  if (p.causal) kv_hi = min(kv_hi, r_last + 1);
+  if (p.causal) kv_hi = min(kv_hi, c_last + 1);
   const int nblk = (kv_hi - kv_lo + 127) / 128;
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
     mbar_init(smem_u32(&bar_q), 1);
     for (int s = 0; s < kSlots; ++s) {
-      mbar_init(smem_u32(&bar_kv_full[s]), 1);
-      mbar_init(smem_u32(&bar_kv_empty[s]), 1);
+      mbar_init(smem_u32(&bar_kv_full[s]), 1);    // the even CTA's: both CTAs' bytes
+      mbar_init(smem_u32(&bar_kv_empty[s]), 1);   // one multicast commit
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(smem_u32(&bar_s[t]), 1);
-      mbar_init(smem_u32(&bar_p[t]), 128);
+      mbar_init(smem_u32(&bar_p[t]), 8);          // the even CTA's: 4 softmax warps per CTA
     }
     mbar_init(smem_u32(&bar_o), 1);
     mbar_init(smem_u32(&bar_drain), 1);
     fence_barrier_init();
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(&tmem_base_sh), 512);
-    tmem_relinquish();
+    tmem_alloc_pair(smem_u32(&tmem_base_sh), 512);
+    tmem_relinquish_pair();
   }
   if (warp == 0 && lane_id() == 0) {
-    tma_prefetch_desc(&tm);
-    if (FP8) tma_prefetch_desc(&tm8);
+    tma_prefetch_desc(FP8 ? &tm8 : &tm);
+    tma_prefetch_desc(FP8 ? &tm8k : &tmk);
+    if (FP8) tma_prefetch_desc(&tm);
   }
   tc_fence_before();
   __syncthreads();
+  cluster_sync();   // both CTAs' barriers exist before any signal crosses
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
 
@@ -256,135 +275,150 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane_id() == 0) {
       const int xq = h * 128, xk = p.d + h * 128, xv = 2 * p.d + h * 128;
       const uint32_t qb = smem_u32(&bar_q);
+      const uint32_t cqb = cluster_addr(qb, 0);
       if (FP8) {   // E4M3 Q | K rows: Q at byte column h*128, K at d + h*128
-        mbar_arrive_expect_tx(qb, 2 * kTile8);
-        tma_load_2d(sQ, &tm8, qb, xq, q0);
-        tma_load_2d(sQ + kTile, &tm8, qb, xq, q0 + 128);
+        if (lead) mbar_arrive_expect_tx(qb, 2 * 2 * kTile8);
+        tma_load_2d_pair(sQ, &tm8, cqb, xq, q0);
+        tma_load_2d_pair(sQ + kTile, &tm8, cqb, xq, q0 + 128);
       } else {
-        mbar_arrive_expect_tx(qb, 2 * kTile);
-        tma_load_2d(sQ, &tm, qb, xq, q0);
-        tma_load_2d(sQ + kBox, &tm, qb, xq + 64, q0);
-        tma_load_2d(sQ + kTile, &tm, qb, xq, q0 + 128);
-        tma_load_2d(sQ + kTile + kBox, &tm, qb, xq + 64, q0 + 128);
+        if (lead) mbar_arrive_expect_tx(qb, 2 * 2 * kTile);
+        tma_load_2d_pair(sQ, &tm, cqb, xq, q0);
+        tma_load_2d_pair(sQ + kBox, &tm, cqb, xq + 64, q0);
+        tma_load_2d_pair(sQ + kTile, &tm, cqb, xq, q0 + 128);
+        tma_load_2d_pair(sQ + kTile + kBox, &tm, cqb, xq + 64, q0 + 128);
       }
-      // pair j = K_j (j < nblk) and V_{j-1} (j >= 1): the two tiles block j's
-      // products read, loaded under one barrier into slot j % 2 (K at the
-      // slot's start, V one tile further)
+      // pair j = this CTA's halves of K_j (j < nblk) and V_{j-1} (j >= 1), the
+      // tiles block j's products read, into slot j % kSlots (K half at the
+      // slot's start, V half one box further)
       bool ok = true;
       int issued = 0;
       for (int j = 0; j <= nblk && ok; ++j) {
-        const int slot = j & 1;
-        if (!mbar_wait(smem_u32(&bar_kv_empty[slot]), ((j >> 1) & 1) ^ 1u, wc)) {
+        const int slot = j % kSlots;
+        if (!mbar_wait(smem_u32(&bar_kv_empty[slot]), ((j / kSlots) & 1) ^ 1u, wc)) {
           ok = false;
           break;
         }
         const uint32_t fb = smem_u32(&bar_kv_full[slot]);
-        const uint32_t dst = sRing + slot * 2 * kTile;
-        const uint32_t kbytes = j < nblk ? (FP8 ? kTile8 : kTile) : 0u;
-        mbar_arrive_expect_tx(fb, kbytes + (j >= 1 ? kTile : 0u));
+        const uint32_t cfb = cluster_addr(fb, 0);
+        const uint32_t dst = sRing + slot * kSlotBytes;
+        const uint32_t kbytes = j < nblk ? (FP8 ? kTile8 / 2 : kBox) : 0u;
+        if (lead) mbar_arrive_expect_tx(fb, 2 * (kbytes + (j >= 1 ? kBox : 0u)));
         if (j < nblk) {
+          const int key0 = kv_lo + j * 128 + int(rank) * 64;
           if (FP8) {
-            tma_load_2d(dst, &tm8, fb, xk, kv_lo + j * 128);
+            tma_load_2d_pair(dst, &tm8k, cfb, xk, key0);
           } else {
-            tma_load_2d(dst, &tm, fb, xk, kv_lo + j * 128);
-            tma_load_2d(dst + kBox, &tm, fb, xk + 64, kv_lo + j * 128);
+            tma_load_2d_pair(dst, &tmk, cfb, xk, key0);
+            tma_load_2d_pair(dst + kHalfBox, &tmk, cfb, xk + 64, key0);
           }
         }
-        if (j >= 1) {
-          tma_load_2d(dst + kTile, &tm, fb, xv, kv_lo + (j - 1) * 128);
-          tma_load_2d(dst + kTile + kBox, &tm, fb, xv + 64, kv_lo + (j - 1) * 128);
-        }
+        if (j >= 1) tma_load_2d_pair(dst + kBox, &tm, cfb, xv + int(rank) * 64, kv_lo + (j - 1) * 128);
         issued = j + 1;
       }
-      // let every copy in flight land before the CTA can exit (earlier pairs
-      // were consumed before their slot was refilled)
-      WaitCtx drain{&abort_flag, p.status, kDrainWaitNs};
-      volatile int no_abort = 0;
-      drain.abort = &no_abort;
-      if (!ok)
-        for (int k = max(0, issued - 2); k < issued; ++k)
-          mbar_wait(smem_u32(&bar_kv_full[k & 1]), (k >> 1) & 1, drain);
-      mbar_wait(qb, 0, drain);
+      // the even CTA lets every copy it armed land before the CTA can exit
+      // (earlier pairs were consumed before their slot was refilled); the odd
+      // CTA's copies count on the even CTA's barriers
+      if (lead) {
+        WaitCtx drain{&abort_flag, p.status, kDrainWaitNs};
+        volatile int no_abort = 0;
+        drain.abort = &no_abort;
+        if (!ok)
+          for (int k = max(0, issued - kSlots); k < issued; ++k)
+            mbar_wait(smem_u32(&bar_kv_full[k % kSlots]), (k / kSlots) & 1, drain);
+        mbar_wait(qb, 0, drain);
+      }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    // The whole warp runs the loop (waits and descriptor arithmetic stay
-    // warp-uniform); one elected lane issues the products and commits.
-    const bool leader = elect_one();
-    auto wait_all = [&](uint32_t bar, uint32_t parity) {
-      return __all_sync(0xffffffffu, mbar_wait(bar, parity, wc));
-    };
-    bool ok = wait_all(smem_u32(&bar_q), 0);
-    // descriptors of Q0, Q1 and of every ring slot read as K (K-major) or V (MN-major)
-    const SDesc dQ0 = sdesc_split(sdesc_sw128(sQ, 16, 1024));
-    const SDesc dQ1 = sdesc_split(sdesc_sw128(sQ + kTile, 16, 1024));
-    // pair slots are 2 kTile apart, V one kTile after K: a descriptor is the
-    // first slot's plus the byte offset / 16
-    const SDesc dK0 = sdesc_split(sdesc_sw128(sRing, 16, 1024));
-    const SDesc dV0 = sdesc_split(sdesc_sw128(sRing + kTile, kBox, 1024));
-    auto dK = [&](int j) { return SDesc{dK0.lo + uint32_t(j & 1) * (2 * kTile >> 4), dK0.hi}; };
-    auto dV = [&](int j) { return SDesc{dV0.lo + uint32_t(j & 1) * (2 * kTile >> 4), dV0.hi}; };
-    auto pair_full = [&](int j) { return smem_u32(&bar_kv_full[j & 1]); };
-    auto pair_empty = [&](int j) { return smem_u32(&bar_kv_empty[j & 1]); };
-    const uint32_t tS0 = tmem, tS1 = tmem + 128, tO0 = tmem + 256, tO1 = tmem + 384;
-    if (ok) ok = wait_all(pair_full(0), 0);
-    if (ok) {
-      tc_fence_after();
-      if (leader) {
-        s_product<FP8>(tS0, dQ0, dK(0));
-        tc_commit(smem_u32(&bar_s[0]));
-        s_product<FP8>(tS1, dQ1, dK(0));
-        tc_commit(smem_u32(&bar_s[1]));
-        tc_commit(pair_empty(0));
-      }
-      __syncwarp();
-    }
-    // block j: P(j-1).V_{j-1} and S(j) for each tile, both tiles from pair j
-    for (int j = 1; j < nblk && ok; ++j) {
-      const uint32_t pph = (j - 1) & 1;
-      ok = wait_all(pair_full(j), (j >> 1) & 1) && wait_all(smem_u32(&bar_p[0]), pph);
-      if (!ok) break;
-      tc_fence_after();
-      if (leader) {
-        pv_product(tO0, tS0 + 64, dV(j), j > 1);
-        s_product<FP8>(tS0, dQ0, dK(j));
-        tc_commit(smem_u32(&bar_s[0]));
-      }
-      __syncwarp();
-      ok = wait_all(smem_u32(&bar_p[1]), pph);
-      if (!ok) break;
-      tc_fence_after();
-      if (leader) {
-        pv_product(tO1, tS1 + 64, dV(j), j > 1);
-        s_product<FP8>(tS1, dQ1, dK(j));
-        tc_commit(smem_u32(&bar_s[1]));
-        tc_commit(pair_empty(j));
-      }
-      __syncwarp();
-    }
-    if (ok) {
-      const int j = nblk;
-      const uint32_t pph = (j - 1) & 1;
-      ok = wait_all(pair_full(j), (j >> 1) & 1) && wait_all(smem_u32(&bar_p[0]), pph);
-      if (ok) {
-        tc_fence_after();
-        if (leader) pv_product(tO0, tS0 + 64, dV(j), j > 1);
-        __syncwarp();
-        ok = wait_all(smem_u32(&bar_p[1]), pph);
-      }
+    if (lead) {
+      // The whole warp runs the loop (waits and descriptor arithmetic stay
+      // warp-uniform); one elected lane issues the products and commits to
+      // the barriers of both CTAs.
+      const bool leader = elect_one();
+      auto wait_all = [&](uint32_t bar, uint32_t parity) {
+        return __all_sync(0xffffffffu, mbar_wait(bar, parity, wc));
+      };
+      auto wait_p = [&](int g, uint32_t parity) {   // arrivals from both CTAs
+        return __all_sync(0xffffffffu, mbar_wait_cluster(smem_u32(&bar_p[g]), parity, wc));
+      };
+      bool ok = wait_all(smem_u32(&bar_q), 0);
+      // descriptors of Q0, Q1 and of every slot read as K (K-major) or V (MN-major)
+      const SDesc dQ0 = sdesc_split(sdesc_sw128(sQ, 16, 1024));
+      const SDesc dQ1 = sdesc_split(sdesc_sw128(sQ + kTile, 16, 1024));
+      // slots are kSlotBytes apart, V one box after K: a descriptor is the
+      // first slot's plus the byte offset / 16
+      const SDesc dK0 = sdesc_split(sdesc_sw128(sRing, 16, 1024));
+      const SDesc dV0 = sdesc_split(sdesc_sw128(sRing + kBox, kBox, 1024));
+      auto dK = [&](int j) {
+        return SDesc{dK0.lo + uint32_t(j % kSlots) * (kSlotBytes >> 4), dK0.hi};
+      };
+      auto dV = [&](int j) {
+        return SDesc{dV0.lo + uint32_t(j % kSlots) * (kSlotBytes >> 4), dV0.hi};
+      };
+      auto pair_full = [&](int j) {
+        return wait_all(smem_u32(&bar_kv_full[j % kSlots]), (j / kSlots) & 1);
+      };
+      auto pair_empty = [&](int j) { return smem_u32(&bar_kv_empty[j % kSlots]); };
+      const uint32_t tS0 = tmem, tS1 = tmem + 128, tO0 = tmem + 256, tO1 = tmem + 384;
+      if (ok) ok = pair_full(0);
       if (ok) {
         tc_fence_after();
         if (leader) {
-          pv_product(tO1, tS1 + 64, dV(j), j > 1);
-          tc_commit(pair_empty(j));
-          tc_commit(smem_u32(&bar_o));
+          s_product<FP8>(tS0, dQ0, dK(0));
+          tc_commit_pair(smem_u32(&bar_s[0]), 0x3);
+          s_product<FP8>(tS1, dQ1, dK(0));
+          tc_commit_pair(smem_u32(&bar_s[1]), 0x3);
+          tc_commit_pair(pair_empty(0), 0x3);
         }
         __syncwarp();
       }
+      // block j: P(j-1).V_{j-1} and S(j) for each tile, both tiles from pair j
+      for (int j = 1; j < nblk && ok; ++j) {
+        const uint32_t pph = (j - 1) & 1;
+        ok = pair_full(j) && wait_p(0, pph);
+        if (!ok) break;
+        tc_fence_after();
+        if (leader) {
+          pv_product(tO0, tS0 + 64, dV(j), j > 1);
+          s_product<FP8>(tS0, dQ0, dK(j));
+          tc_commit_pair(smem_u32(&bar_s[0]), 0x3);
+        }
+        __syncwarp();
+        ok = wait_p(1, pph);
+        if (!ok) break;
+        tc_fence_after();
+        if (leader) {
+          pv_product(tO1, tS1 + 64, dV(j), j > 1);
+          s_product<FP8>(tS1, dQ1, dK(j));
+          tc_commit_pair(smem_u32(&bar_s[1]), 0x3);
+          tc_commit_pair(pair_empty(j), 0x3);
+        }
+        __syncwarp();
+      }
+      if (ok) {
+        const int j = nblk;
+        const uint32_t pph = (j - 1) & 1;
+        ok = pair_full(j) && wait_p(0, pph);
+        if (ok) {
+          tc_fence_after();
+          if (leader) pv_product(tO0, tS0 + 64, dV(j), j > 1);
+          __syncwarp();
+          ok = wait_p(1, pph);
+        }
+        if (ok) {
+          tc_fence_after();
+          if (leader) {
+            pv_product(tO1, tS1 + 64, dV(j), j > 1);
+            tc_commit_pair(pair_empty(j), 0x3);
+            tc_commit_pair(smem_u32(&bar_o), 0x3);
+          }
+          __syncwarp();
+        }
+      }
+      // let every product issued so far finish before either CTA frees tensor memory
+      if (leader) tc_commit_pair(smem_u32(&bar_drain), 0x3);
+      __syncwarp();
     }
-    // let every product issued so far finish before the CTA frees tensor memory
-    if (leader) tc_commit(smem_u32(&bar_drain));
-    __syncwarp();
     WaitCtx drain{&abort_flag, p.status, kDrainWaitNs};
     volatile int no_abort = 0;
     drain.abort = &no_abort;
@@ -399,7 +433,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = uint32_t(q * 32) << 16;
     const uint32_t tS = tmem + g * 128 + lane_off;
     const uint32_t tO = tmem + 256 + g * 128 + lane_off;
-    const uint32_t bs = smem_u32(&bar_s[g]), bp = smem_u32(&bar_p[g]);
+    const uint32_t bs = smem_u32(&bar_s[g]);
+    const uint32_t bp = cluster_addr(smem_u32(&bar_p[g]), 0);   // the even CTA's
     // keys visible to this row: its segment, up to itself when causal
     int row_lo = 0, row_hi = p.L;
     if (p.n_seg > 0) {
@@ -494,9 +529,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       unf2(acc[0], a0, a1);
       unf2(acc[1], b0, b1);
       l += (a0 + a1) + (b0 + b1);
+      // P (and a rescaled O) are in tensor memory: one arrival per warp
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(bp);
+      __syncwarp();
+      if (lane_id() == 0) mbar_arrive_cluster(bp);
     }
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_o), 0, wc));
     if (ok) {
@@ -527,22 +564,27 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  cluster_sync();   // neither CTA leaves while the other may still signal it
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem, 512);
+  if (warp == 1) tmem_dealloc_pair(tmem, 512);
 }
 
 }  // namespace
 
 cudaError_t launch_attention(const AttnArgs& a, const DevCtx& ctx, cudaStream_t st) {
   const int d = a.H * 128;
-  CUtensorMap tm, tm8;
+  // Q and V in 128-row boxes, K in 64-row boxes (each CTA of a pair holds 64 keys)
+  CUtensorMap tm, tmk, tm8, tm8k;
   if (!make_tmap_bf16_2d(&tm, a.qkv, a.L, 3 * d, 3 * d, 128, 64)) return cudaErrorInvalidValue;
+  if (!make_tmap_bf16_2d(&tmk, a.qkv, a.L, 3 * d, 3 * d, 64, 64)) return cudaErrorInvalidValue;
   if (a.fp8) {
     if (a.n_seg != 0 || a.qk8 == nullptr || a.sq == nullptr || a.sk == nullptr)
       return cudaErrorInvalidValue;
     if (!make_tmap_u8_2d(&tm8, a.qk8, a.L, 2 * d, 2 * d, 128)) return cudaErrorInvalidValue;
+    if (!make_tmap_u8_2d(&tm8k, a.qk8, a.L, 2 * d, 2 * d, 64)) return cudaErrorInvalidValue;
   } else {
     tm8 = tm;   // unused
+    tm8k = tmk;
   }
   AttnDev p{};
   p.O = static_cast<__nv_bfloat16*>(a.O);
@@ -552,7 +594,7 @@ cudaError_t launch_attention(const AttnArgs& a, const DevCtx& ctx, cudaStream_t 
   p.d = d;
   p.causal = a.causal;
   p.scale_log2 = a.sm_scale * 1.4426950408889634f;
-  p.num_pairs = (a.L + 255) / 256;
+  p.num_quads = (a.L + 511) / 512;
   p.status = ctx.status;
   p.wait_ns = ctx.wait_ns;
   p.n_seg = a.n_seg;
@@ -563,8 +605,20 @@ cudaError_t launch_attention(const AttnArgs& a, const DevCtx& ctx, cudaStream_t 
   auto kernel = a.fp8 ? attn_fwd_kernel<true> : attn_fwd_kernel<false>;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmem));
   if (e != cudaSuccess) return e;
-  const long long grid = (long long)p.num_pairs * a.H;
-  kernel<<<unsigned(grid), kThreads, kSmem, st>>>(tm, tm8, p);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(unsigned(2LL * p.num_quads * a.H));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kernel, tm, tmk, tm8, tm8k, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
