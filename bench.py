@@ -380,6 +380,18 @@ def run_gpu(args, cfg):
     torch.cuda.synchronize(dev)
     varlen_ms = vev[0].elapsed_time(vev[1]) / 5
     varlen_flops = 4.0 * d * sum((cu[i + 1] - cu[i]) ** 2 for i in range(3))
+
+    # ---- the causal option of the same attention call (key index <= query
+    # index in packed order) on the same rotated qkv, timed on its own
+    h3.h3_joint_attn_fwd(qkv_ws, L, H, 128, 1, None, o_var, stream=stream)
+    cev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    cev[0].record(stream)
+    for _ in range(5):
+        h3.h3_joint_attn_fwd(qkv_ws, L, H, 128, 1, None, o_var, stream=stream)
+    cev[1].record(stream)
+    torch.cuda.synchronize(dev)
+    causal_ms = cev[0].elapsed_time(cev[1]) / 5
+    causal_flops = 4.0 * d * L * (L + 1) / 2.0
     del o_var
 
     # ---- the standalone 3D RoPE call (h3_mrope_apply, in place on Q and K of the
@@ -562,6 +574,11 @@ def run_gpu(args, cfg):
                                  "tflops": varlen_flops / (varlen_ms * 1e-3) / 1e12,
                                  "frac_of_sustained_bf16_peak":
                                      varlen_flops / (varlen_ms * 1e-3) / 1e12 / peak},
+        "attn_causal": {"ms": causal_ms, "flops": causal_flops,
+                        "tflops": causal_flops / (causal_ms * 1e-3) / 1e12,
+                        "frac_of_sustained_bf16_peak":
+                            causal_flops / (causal_ms * 1e-3) / 1e12 / peak,
+                        "note": "unmasked pairs only: 4 d L (L + 1) / 2 FLOPs"},
         "mlp_block": {"hidden": hid, "ms": mlp_ms,
                       "tflops": mlp_flops / (mlp_ms * 1e-3) / 1e12,
                       "frac_of_sustained_bf16_peak": mlp_flops / (mlp_ms * 1e-3) / 1e12 / peak},
