@@ -64,6 +64,26 @@ def assert_parity(got, ref, what: str, max_rel_rms: float = MAX_REL_RMS,
     return mx, mr
 
 
+def assert_parity_rows(got, ref, what: str, max_rel_rms: float = MAX_REL_RMS,
+                       mean_rel: float = MEAN_REL):
+    """assert_parity with each row held to its own RMS: for causal attention,
+    where row i is a softmax over its own i + 1 keys and the rows' output
+    scales differ by the square root of their key counts (1 to 58,758 keys at
+    full size).  Per element |err| <= max_rel_rms * RMS(ref row) + 2^-8 |ref|;
+    the mean relative error is over all rows."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    _, mr = stats(got, ref)
+    rrms = np.sqrt(np.mean(ref * ref, axis=1, keepdims=True))
+    bound = max_rel_rms * rrms + BF16_U * np.abs(ref)
+    excess = float(np.max(np.abs(got - ref) - bound))
+    worst = float(np.max(np.abs(got - ref) / np.maximum(rrms, 1e-300)))
+    assert excess <= 0.0 and mr <= mean_rel, (
+        f"{what}: max |err| / row RMS = {worst:.3e} (bound {max_rel_rms} + 2^-8|ref|, worst "
+        f"excess {excess:.3e}), mean rel = {mr:.3e} (<= {mean_rel})")
+    return worst, mr
+
+
 def slice_rows(L: int, n_text: int) -> np.ndarray:
     """The 1,024 query rows of the full-size spot check: rows 0..127 (text),
     one video row every 75 tokens from the first video token (768 rows that

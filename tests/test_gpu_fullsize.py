@@ -14,7 +14,7 @@ import torch
 
 import oracle as orc
 from h3inputs import CONFIGS, attention_qkv, block_inputs, random_rows
-from tests._parity import CHAIN_MAX_REL_RMS, assert_parity, slice_rows, to64
+from tests._parity import CHAIN_MAX_REL_RMS, assert_parity, assert_parity_rows, slice_rows, to64
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -35,6 +35,29 @@ def test_full_attention_slice_rows(h3):
     ro, rl = orc.attention(to64(qkv), H, 128, rows=rows)
     ridx = torch.from_numpy(rows).to(DEV)
     assert_parity(to64(O[ridx]), ro, "full-size attention, slice rows")
+    np.testing.assert_allclose(to64(lse[:, ridx]), rl, atol=2e-2, rtol=1e-3)
+
+
+def test_full_causal_attention_slice_rows(h3):
+    """The causal option at full length on the same slice: each row sees the
+    keys up to itself in packed order ("多模态强化学习工程解析…", 三 目标模型),
+    so the slice's rows see from one key (row 0) to all 58,758 (the last
+    row), and every row's last key block is cut by the diagonal.  Each row is
+    held to its own RMS (test_causal_bound_cpu.py shows why the slice-wide
+    RMS cannot hold for the rows with a few keys)."""
+    c = CONFIGS["full"]
+    L, H = c.L, c.n_heads
+    qkv = attention_qkv(L, H, seed=57)
+    dev = qkv.to(DEV)
+    O = torch.full((L, H * 128), float("nan"), dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty(H, L, dtype=torch.float32, device=DEV)
+    h3.h3_joint_attn_fwd(dev, L, H, 128, 1, 1 / math.sqrt(128), O, lse)
+    assert h3.h3_sync_status() == 0
+    assert torch.isfinite(O.float()).all()
+    rows = slice_rows(L, c.n_text)
+    ro, rl = orc.attention(to64(qkv), H, 128, causal=True, rows=rows)
+    ridx = torch.from_numpy(rows).to(DEV)
+    assert_parity_rows(to64(O[ridx]), ro, "full-size causal attention, slice rows")
     np.testing.assert_allclose(to64(lse[:, ridx]), rl, atol=2e-2, rtol=1e-3)
 
 
