@@ -75,6 +75,8 @@ typedef int h3_status;
 #define H3_ERR_TIMEOUT 4       /* a kernel gave up on a bounded wait (device status) */
 #define H3_ERR_BAD_INDEX 5     /* a modality id >= n_mod was met (device status) */
 #define H3_ERR_WORKSPACE 6     /* workspace smaller than h3_workspace_size() */
+#define H3_ERR_OUT_OF_BOUNDS 7 /* checked build only: a kernel index fell outside its
+                                  buffer; the access was skipped (device status) */
 
 /* Same handle as cudaStream_t; NULL is the legacy default stream. */
 typedef struct CUstream_st* h3_stream_t;
@@ -385,7 +387,8 @@ h3_status h3_attn_block_fwd_noalloc(const h3_block_desc* desc, const uint16_t* x
 
 /*
  * Synchronise `stream`, then report and clear the current device's status
- * word: H3_OK, H3_ERR_TIMEOUT, H3_ERR_BAD_INDEX or H3_ERR_CUDA.
+ * word: H3_OK, H3_ERR_TIMEOUT, H3_ERR_BAD_INDEX, H3_ERR_OUT_OF_BOUNDS (checked
+ * build) or H3_ERR_CUDA.
  */
 h3_status h3_sync_status(h3_stream_t stream);
 
@@ -402,6 +405,28 @@ void h3_set_wait_limit_ns(uint64_t limit_ns);
  * must run out and the following h3_sync_status() must return H3_ERR_TIMEOUT.
  */
 h3_status h3_selftest_wait_timeout(uint64_t limit_ns, h3_stream_t stream);
+
+/*
+ * The checked build.  The library can be compiled with H3_CHECKED defined
+ * (libh3attn_checked.so, joint_audio_video_gb300/build.py, build(checked=True)):
+ * then every global-memory load or store that a kernel addresses itself (all
+ * but the TMA copies, which the hardware bounds) first tests its row and
+ * column against the extents of its buffer; a test that fails records
+ * H3_ERR_OUT_OF_BOUNDS in the device status word, skips the access, and the
+ * kernel goes on.  Results are bit-identical to the normal build's.  This is a
+ * debugging aid with no counterpart on the pages (the pages' lesson is that
+ * kernel failures at this sequence length are silent: "Joint Audio-Video
+ * Generation in Production", §6 Boundary Trimming for Packed Attention).
+ *
+ * h3_checked_build(): 1 in the checked build, 0 otherwise.
+ * h3_selftest_bounds_check(): in the checked build, launches one thread that
+ * addresses element 1 of a one-element buffer through the checked path, so the
+ * following h3_sync_status() must return H3_ERR_OUT_OF_BOUNDS (nothing is
+ * written); in the normal build it returns H3_ERR_UNSUPPORTED and launches
+ * nothing.
+ */
+int32_t h3_checked_build(void);
+h3_status h3_selftest_bounds_check(h3_stream_t stream);
 
 #ifdef __cplusplus
 }

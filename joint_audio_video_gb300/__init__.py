@@ -26,15 +26,18 @@ __all__ = [
     "h3_quantize_rows_fp8", "h3_gemm_fp8", "h3_workspace_size_fp8", "h3_attn_block_fwd_fp8",
     "h3_mlp_workspace_size_fp8", "h3_mlp_block_fwd_fp8",
     "h3_attn_workspace_size_fp8", "h3_quantize_qk_fp8", "h3_joint_attn_fwd_fp8",
-    "NOALLOC_SCRATCH_BYTES", "EXPORTED_SYMBOLS",
+    "NOALLOC_SCRATCH_BYTES", "EXPORTED_SYMBOLS", "load_checked", "h3_checked_build",
+    "h3_selftest_bounds_check",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 lib_path = os.path.join(_HERE, "libh3attn.so")
+checked_lib_path = os.path.join(_HERE, "libh3attn_checked.so")
 
 H3_OK = 0
 STATUS_NAMES = {0: "H3_OK", 1: "H3_ERR_INVALID_ARG", 2: "H3_ERR_UNSUPPORTED", 3: "H3_ERR_CUDA",
-                4: "H3_ERR_TIMEOUT", 5: "H3_ERR_BAD_INDEX", 6: "H3_ERR_WORKSPACE"}
+                4: "H3_ERR_TIMEOUT", 5: "H3_ERR_BAD_INDEX", 6: "H3_ERR_WORKSPACE",
+                7: "H3_ERR_OUT_OF_BOUNDS"}
 
 EXPORTED_SYMBOLS = (
     "h3_status_string", "h3_version", "h3_build_packed_layout", "h3_adaln_modulate",
@@ -46,6 +49,7 @@ EXPORTED_SYMBOLS = (
     "h3_quantize_rows_fp8", "h3_gemm_fp8", "h3_workspace_size_fp8", "h3_attn_block_fwd_fp8",
     "h3_mlp_workspace_size_fp8", "h3_mlp_block_fwd_fp8",
     "h3_attn_workspace_size_fp8", "h3_quantize_qk_fp8", "h3_joint_attn_fwd_fp8",
+    "h3_checked_build", "h3_selftest_bounds_check",
 )
 
 # Workspace the library keeps per GPU for h3_attn_block_fwd_noalloc.
@@ -137,6 +141,8 @@ def _sig(lib):
     lib.h3_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
     lib.h3_set_wait_limit_ns.restype = None
     lib.h3_selftest_wait_timeout.argtypes = [ctypes.c_uint64, _P]
+    lib.h3_checked_build.argtypes = []
+    lib.h3_selftest_bounds_check.argtypes = [_P]
     for name in EXPORTED_SYMBOLS:
         if name not in ("h3_status_string", "h3_version", "h3_set_wait_limit_ns"):
             getattr(lib, name).restype = ctypes.c_int
@@ -153,6 +159,20 @@ def load() -> ctypes.CDLL:
         _sig(lib)
         _lib = lib
     return _lib
+
+
+def load_checked() -> ctypes.CDLL:
+    """The checked library (libh3attn_checked.so, built in-tree by
+    ``build.build(checked=True)``): the same entry points, every kernel's own
+    global accesses bounds-tested (a failed test reports H3_ERR_OUT_OF_BOUNDS
+    through h3_sync_status).  Loaded next to, not instead of, the library;
+    call its entry points on the returned handle."""
+    if not os.path.exists(checked_lib_path):
+        raise RuntimeError(f"{checked_lib_path} is missing: build it with "
+                           "joint_audio_video_gb300.build.build(checked=True) (needs nvcc)")
+    lib = ctypes.CDLL(checked_lib_path)
+    _sig(lib)
+    return lib
 
 
 def _addr(t) -> Optional[int]:
@@ -389,3 +409,14 @@ def h3_set_wait_limit_ns(limit_ns: int) -> None:
 def h3_selftest_wait_timeout(limit_ns: int, stream=None) -> None:
     _check("h3_selftest_wait_timeout",
            load().h3_selftest_wait_timeout(int(limit_ns), _stream(stream)))
+
+
+def h3_checked_build() -> bool:
+    return bool(load().h3_checked_build())
+
+
+def h3_selftest_bounds_check(stream=None) -> int:
+    """Returns the entry point's status: H3_ERR_UNSUPPORTED (2) in the normal
+    build, which launches nothing; in the checked build, after the launch, the
+    next h3_sync_status() reports H3_ERR_OUT_OF_BOUNDS."""
+    return int(load().h3_selftest_bounds_check(_stream(stream)))

@@ -3,7 +3,10 @@
 Each translation unit is compiled in parallel into ``_obj/``; the shared
 library links the CUDA runtime statically, so it has no load-time dependency
 on a GPU driver.  A source newer than the library (or a changed flag set)
-triggers a rebuild.
+triggers a rebuild.  ``build(checked=True)`` builds the checked library
+(``libh3attn_checked.so`` from ``_obj_checked/``, compiled with H3_CHECKED:
+every global access a kernel addresses itself is tested against its buffer's
+extents first).
 """
 from __future__ import annotations
 
@@ -19,6 +22,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OBJ = os.path.join(PKG, "_obj")
 LIB = os.path.join(PKG, "libh3attn.so")
+OBJ_CHECKED = os.path.join(PKG, "_obj_checked")
+LIB_CHECKED = os.path.join(PKG, "libh3attn_checked.so")
 INCLUDE = os.path.join(ROOT, "include")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -36,9 +41,9 @@ def _nvcc() -> str:
     raise RuntimeError("nvcc not found: the h3attn CUDA library cannot be built")
 
 
-def _stamp() -> str:
+def _stamp(flags) -> str:
     h = hashlib.sha256()
-    h.update(" ".join(ARCH + CUFLAGS).encode())
+    h.update(" ".join(ARCH + flags).encode())
     for name in SOURCES + HEADERS:
         with open(os.path.join(CSRC, name), "rb") as f:
             h.update(name.encode())
@@ -48,40 +53,44 @@ def _stamp() -> str:
     return h.hexdigest()
 
 
-def _compile(src: str, verbose: bool) -> str:
-    obj = os.path.join(OBJ, os.path.splitext(src)[0] + ".o")
-    cmd = [_nvcc(), *ARCH, *CUFLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
+def _compile(src: str, verbose: bool, obj_dir: str, flags) -> str:
+    obj = os.path.join(obj_dir, os.path.splitext(src)[0] + ".o")
+    cmd = [_nvcc(), *ARCH, *flags, "-c", os.path.join(CSRC, src), "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")
-    with open(os.path.join(OBJ, os.path.splitext(src)[0] + ".ptxas.txt"), "w") as f:
+    with open(os.path.join(obj_dir, os.path.splitext(src)[0] + ".ptxas.txt"), "w") as f:
         f.write(r.stderr)
     if verbose:
         sys.stderr.write(r.stderr)
     return obj
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile the library if it is missing or stale; return its path."""
-    os.makedirs(OBJ, exist_ok=True)
-    stamp_file = os.path.join(OBJ, "stamp")
-    stamp = _stamp()
-    if not force and os.path.exists(LIB) and os.path.exists(stamp_file):
+def build(force: bool = False, verbose: bool = False, checked: bool = False) -> str:
+    """Compile the library (or, with ``checked``, the checked library) if it is
+    missing or stale; return its path."""
+    obj_dir, lib = (OBJ_CHECKED, LIB_CHECKED) if checked else (OBJ, LIB)
+    flags = CUFLAGS + (["-DH3_CHECKED"] if checked else [])
+    os.makedirs(obj_dir, exist_ok=True)
+    stamp_file = os.path.join(obj_dir, "stamp")
+    stamp = _stamp(flags)
+    if not force and os.path.exists(lib) and os.path.exists(stamp_file):
         with open(stamp_file) as f:
             if f.read().strip() == stamp:
-                return LIB
+                return lib
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, verbose), SOURCES))
-    tmp = LIB + ".tmp"
+        objs = list(ex.map(lambda s: _compile(s, verbose, obj_dir, flags), SOURCES))
+    tmp = lib + ".tmp"
     cmd = [_nvcc(), *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
+    os.replace(tmp, lib)
     with open(stamp_file, "w") as f:
         f.write(stamp)
-    return LIB
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv,
+                checked="--checked" in sys.argv))

@@ -79,9 +79,13 @@ __global__ void __launch_bounds__(kThreads)
   auto issue = [&](int k) {   // row k of this CTA into ring slot k % stages
     const int s = k % stages;
     const uint32_t bar = smem_u32(&full[s]);
-    mbar_arrive_expect_tx(bar, row_bytes);
-    bulk_load_1d(smem_u32(ring + size_t(s) * row_bytes),
-                 x + size_t(blockIdx.x + size_t(k) * G) * nvec, row_bytes, bar);
+    const size_t row = blockIdx.x + size_t(k) * G;
+    if (H3_IN(row < size_t(L), status)) {
+      mbar_arrive_expect_tx(bar, row_bytes);
+      bulk_load_1d(smem_u32(ring + size_t(s) * row_bytes), x + row * nvec, row_bytes, bar);
+    } else {
+      mbar_arrive(bar);   // checked build: the row is skipped, the slot completes
+    }
   };
   int issued = 0;
   if (threadIdx.x == 0)
@@ -108,7 +112,8 @@ __global__ void __launch_bounds__(kThreads)
       const int c = threadIdx.x + i * kThreads;
       v[i] = c < nvec ? xr[c] : make_uint4(0, 0, 0, 0);
     }
-    const int m = mod[row];
+    const bool row_ok = H3_IN(row < size_t(L), status);
+    const int m = row_ok ? int(mod[row]) : 0;
 
     // eight independent partial sums per pass: short dependency chains
     float part[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
@@ -145,6 +150,7 @@ __global__ void __launch_bounds__(kThreads)
     const float rstd = rsqrtf(block_sum(q, red[1]) * inv_d + eps);
 
     uint4* yr = y + row * nvec;
+    if (!row_ok) continue;   // checked build only
     if (m >= n_mod) {  // uniform across the CTA
       if (threadIdx.x == 0) atomicCAS(status, H3_DEV_OK, H3_DEV_BAD_INDEX);
       const uint4 nan4 = make_uint4(0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u);

@@ -439,18 +439,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     int row_lo = 0, row_hi = p.L;
     if (p.n_seg > 0) {
       const int sg = segment_of(p, min(qi, p.L - 1));
-      row_lo = p.cu[sg];
-      row_hi = p.cu[sg + 1];
+      if (H3_IN(sg >= 0 && sg < p.n_seg, p.status)) {
+        row_lo = p.cu[sg];
+        row_hi = p.cu[sg + 1];
+      }
     }
     if (p.causal) row_hi = min(row_hi, qi + 1);
     float m_used = -INFINITY, l = 0.f;
     // exponent constant: sm_scale log2(e), times the row's Q scale for fp8 scores
     float c_row = p.scale_log2;
-    if (FP8) c_row *= p.sq[size_t(h) * p.L + min(qi, p.L - 1)];
+    const bool head_ok = H3_IN(h < p.H, p.status);   // column h*128 of O, rows h of lse, sq, sk
+    if (FP8 && head_ok) c_row *= p.sq[size_t(h) * p.L + min(qi, p.L - 1)];
     bool ok = true;
     for (int j = 0; j < nblk; ++j) {
       // ... and the key block's K scale (fp8 scores have kv_lo = 0)
-      const float c = FP8 ? c_row * p.sk[size_t(h) * p.nkb + j] : c_row;
+      const float c =
+          FP8 && head_ok && H3_IN(j < p.nkb, p.status) ? c_row * p.sk[size_t(h) * p.nkb + j] : c_row;
       ok = __all_sync(0xffffffffu, mbar_wait(bs, j & 1, wc));
       if (!ok) break;
       tc_fence_after();
@@ -545,7 +549,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t o[32];
         tmem_ld32(tO + c * 32, o);
         tmem_ld_wait(o);
-        if (qi < p.L) {
+        if (qi < p.L && head_ok) {
           uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
@@ -557,7 +561,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (p.lse != nullptr && qi < p.L)
+      if (p.lse != nullptr && qi < p.L && head_ok)
         p.lse[size_t(h) * p.L + qi] = (m_used + __log2f(l)) * 0.69314718055994531f;
     }
   }

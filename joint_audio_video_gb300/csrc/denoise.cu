@@ -29,6 +29,7 @@ __global__ void __launch_bounds__(256)
   for (size_t i = blockIdx.x * size_t(blockDim.x) + threadIdx.x; i < n_vec;
        i += size_t(gridDim.x) * blockDim.x) {
     const size_t r = i / size_t(vec_per_row);
+    if (!H3_IN((r + 1) * size_t(vec_per_row) <= n_vec, status)) continue;   // row r of L
     const int m = mod[r];
     if (m >= n_mod) {                       // leave the row as it is and report
       atomicCAS(status, H3_DEV_OK, H3_DEV_BAD_INDEX);

@@ -83,6 +83,8 @@ __device__ __forceinline__ void epilogue_chunk(const GemmDev& p, const RopeTable
                                                uint32_t (&r)[32], int grow, int gc,
                                                const int32_t (&pr)[3], int m, float sa,
                                                uint32_t (&pk)[16]) {
+  // columns gc .. gc + 31 of C, x_res, gate and b_scale
+  if (!H3_IN(gc >= 0 && gc + 32 <= p.N, p.status)) return;
   float v[32];
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);

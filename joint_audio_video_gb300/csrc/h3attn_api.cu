@@ -148,6 +148,18 @@ __global__ void wait_selftest_kernel(int* status, uint64_t limit_ns) {
 
 }  // namespace
 
+// One-element target of the bounds self-test.
+__device__ int g_selftest_cell;
+
+// One thread addresses element `i` of the one-element g_selftest_cell through
+// the checked path: with i >= 1 the access is skipped and the status word
+// records H3_DEV_OUT_OF_BOUNDS (checked build only; the normal build never
+// launches it).
+__global__ void bounds_selftest_kernel(int i, int* status) {
+  int* cell = &g_selftest_cell;
+  if (H3_IN(i >= 0 && i < 1, status)) cell[i] = 1;
+}
+
 cudaError_t launch_wait_selftest(const DevCtx& ctx, cudaStream_t st) {
   wait_selftest_kernel<<<1, 32, 0, st>>>(ctx.status, ctx.wait_ns);
   return cudaGetLastError();
@@ -168,6 +180,7 @@ const char* h3_status_string(h3_status s) {
     case H3_ERR_TIMEOUT: return "a kernel gave up on a bounded wait";
     case H3_ERR_BAD_INDEX: return "modality id out of range";
     case H3_ERR_WORKSPACE: return "workspace too small";
+    case H3_ERR_OUT_OF_BOUNDS: return "a kernel index fell outside its buffer (checked build)";
     default: return "unknown status";
   }
 }
@@ -830,6 +843,7 @@ h3_status h3_sync_status(h3_stream_t stream) {
     case H3_DEV_OK: return H3_OK;
     case H3_DEV_TIMEOUT: return H3_ERR_TIMEOUT;
     case H3_DEV_BAD_INDEX: return H3_ERR_BAD_INDEX;
+    case H3_DEV_OUT_OF_BOUNDS: return H3_ERR_OUT_OF_BOUNDS;
     default: return H3_ERR_CUDA;
   }
 }
@@ -842,6 +856,27 @@ h3_status h3_selftest_wait_timeout(uint64_t limit_ns, h3_stream_t stream) {
   ctx.wait_ns = limit_ns;
   return finish(launched(launch_wait_selftest(ctx, reinterpret_cast<cudaStream_t>(stream))),
                 stream);
+}
+
+int32_t h3_checked_build(void) {
+#ifdef H3_CHECKED
+  return 1;
+#else
+  return 0;
+#endif
+}
+
+h3_status h3_selftest_bounds_check(h3_stream_t stream) {
+  const Trace trace_("h3_selftest_bounds_check");
+#ifdef H3_CHECKED
+  DevCtx ctx;
+  if (h3_status s = dev_ctx(&ctx)) return s;
+  bounds_selftest_kernel<<<1, 1, 0, reinterpret_cast<cudaStream_t>(stream)>>>(1, ctx.status);
+  return finish(launched(cudaGetLastError()), stream);
+#else
+  (void)stream;
+  return H3_ERR_UNSUPPORTED;
+#endif
 }
 
 }  // extern "C"

@@ -40,14 +40,14 @@ constexpr int kTokens = 4;
 
 __global__ void __launch_bounds__(kThreads)
     mrope_kernel(uint4* __restrict__ qkv, const int32_t* __restrict__ pos, int L, int d,
-                 const __grid_constant__ RopeTable rt) {
+                 const __grid_constant__ RopeTable rt, int* status) {
   __shared__ float2 cs[kTokens][64];
   const int tok0 = blockIdx.x * kTokens;
   for (int i = threadIdx.x; i < kTokens * 64; i += kThreads) {
     const int t = i >> 6, k = i & 63;
     const int n = tok0 + t;
     float s = 0.f, c = 1.f;
-    if (n < L) {
+    if (n < L && H3_IN(rt.axis[k] >= 0 && rt.axis[k] < 3, status)) {
       const float ang = float(pos[size_t(n) * 3 + rt.axis[k]]) * rt.inv_freq[k];
       sincosf(ang, &s, &c);
     }
@@ -60,6 +60,8 @@ __global__ void __launch_bounds__(kThreads)
     const int t = i / vec_qk, v = i - t * vec_qk;
     const int n = tok0 + t;
     if (n >= L) break;
+    // the Q|K part of row n (its first 2d of 3d columns), pairs k0 .. k0 + 3 of the table
+    if (!H3_IN(v < vec_qk && ((v * 8) & 127) / 2 + 3 < 64, status)) continue;
     uint4* p = qkv + size_t(n) * row_vec + v;
     uint4 w = *p;
     const int k0 = ((v * 8) & 127) >> 1;   // first pair of this vector inside its head
@@ -79,9 +81,9 @@ __global__ void __launch_bounds__(kThreads)
 
 cudaError_t launch_mrope(void* qkv, const int32_t* pos, int L, int n_heads, const RopeTable& rt,
                          const DevCtx& ctx, cudaStream_t st) {
-  (void)ctx;
   const int grid = (L + kTokens - 1) / kTokens;
-  mrope_kernel<<<grid, kThreads, 0, st>>>(static_cast<uint4*>(qkv), pos, L, n_heads * 128, rt);
+  mrope_kernel<<<grid, kThreads, 0, st>>>(static_cast<uint4*>(qkv), pos, L, n_heads * 128, rt,
+                                          ctx.status);
   return cudaGetLastError();
 }
 

@@ -16,7 +16,20 @@
 namespace h3 {
 
 // Device status word values (first error wins).
-enum : int { H3_DEV_OK = 0, H3_DEV_TIMEOUT = 1, H3_DEV_BAD_INDEX = 2 };
+enum : int { H3_DEV_OK = 0, H3_DEV_TIMEOUT = 1, H3_DEV_BAD_INDEX = 2, H3_DEV_OUT_OF_BOUNDS = 3 };
+
+// Bounds checks of the checked build (compiled with H3_CHECKED): H3_IN(ok,
+// status) is `ok`, and a false `ok` records H3_DEV_OUT_OF_BOUNDS so the caller
+// skips the access.  In the normal build it is `true` and compiles away.
+__device__ __forceinline__ bool h3_in_bounds(bool ok, int* status) {
+  if (!ok) atomicCAS(status, 0, 3);
+  return ok;
+}
+#ifdef H3_CHECKED
+#define H3_IN(ok, status) ::h3::h3_in_bounds((ok), (status))
+#else
+#define H3_IN(ok, status) true
+#endif
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

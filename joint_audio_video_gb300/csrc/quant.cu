@@ -25,10 +25,11 @@ __device__ __forceinline__ uint16_t e4m3x2(float lo, float hi) {
 }
 
 __global__ void __launch_bounds__(kThreads)
-    quantize_rows_kernel(const uint4* __restrict__ x, int K, uint2* __restrict__ q,
-                         float* __restrict__ scale) {
+    quantize_rows_kernel(const uint4* __restrict__ x, int R, int K, uint2* __restrict__ q,
+                         float* __restrict__ scale, int* status) {
   __shared__ float red[kThreads / 32];
   const size_t row = blockIdx.x;
+  if (!H3_IN(row < size_t(R), status)) return;   // uniform across the CTA
   const int nvec = K >> 3;
   const uint4* xr = x + row * nvec;
   float am = 0.f;
@@ -92,9 +93,11 @@ __device__ __forceinline__ uint2 e4m3x8(const uint4& v, float inv) {
 
 __global__ void __launch_bounds__(kThreads)
     quantize_qk_kernel(const uint4* __restrict__ qkv, int L, int H, int nkb,
-                       uint2* __restrict__ qk8, float* __restrict__ sq, float* __restrict__ sk) {
+                       uint2* __restrict__ qk8, float* __restrict__ sq, float* __restrict__ sk,
+                       int* status) {
   __shared__ float red[kThreads / 32];
   const int b = blockIdx.x % nkb, h = blockIdx.x / nkb;
+  if (!H3_IN(h < H, status)) return;   // uniform across the CTA
   const int c = threadIdx.x & 15;                  // 8-element chunk of the head's 128 dims
   const size_t d = size_t(H) * 128;
   const size_t in_row = 3 * d / 8, out_row = 2 * d / 8;   // row pitches in uint4 / uint2
@@ -140,18 +143,16 @@ __global__ void __launch_bounds__(kThreads)
 
 cudaError_t launch_quantize_qk(const void* qkv, int L, int H, void* qk8, float* sq, float* sk,
                                const DevCtx& ctx, cudaStream_t st) {
-  (void)ctx;
   const int nkb = (L + kQkRows - 1) / kQkRows;
   quantize_qk_kernel<<<unsigned(nkb) * unsigned(H), kThreads, 0, st>>>(
-      static_cast<const uint4*>(qkv), L, H, nkb, static_cast<uint2*>(qk8), sq, sk);
+      static_cast<const uint4*>(qkv), L, H, nkb, static_cast<uint2*>(qk8), sq, sk, ctx.status);
   return cudaGetLastError();
 }
 
 cudaError_t launch_quantize_rows(const void* x, int R, int K, void* q, float* scale,
                                  const DevCtx& ctx, cudaStream_t st) {
-  (void)ctx;
-  quantize_rows_kernel<<<R, kThreads, 0, st>>>(static_cast<const uint4*>(x), K,
-                                               static_cast<uint2*>(q), scale);
+  quantize_rows_kernel<<<R, kThreads, 0, st>>>(static_cast<const uint4*>(x), R, K,
+                                               static_cast<uint2*>(q), scale, ctx.status);
   return cudaGetLastError();
 }
 

@@ -25,12 +25,13 @@ def lib():
 def _declared():
     with open(os.path.join(ROOT, "include", "h3attn.h")) as f:
         text = f.read()
-    return sorted(set(re.findall(r"^\s*(?:const char\*|h3_status|void)\s+(h3_\w+)\s*\(", text, re.M)))
+    return sorted(set(re.findall(r"^\s*(?:const char\*|h3_status|void|int32_t)\s+(h3_\w+)\s*\(",
+                                 text, re.M)))
 
 
 def test_library_exports_every_declared_entry_point(lib):
     names = _declared()
-    assert len(names) == 28, names
+    assert len(names) == 30, names
     raw = ctypes.CDLL(lib.lib_path)
     for n in names:
         assert hasattr(raw, n), f"{n} declared but not exported"
