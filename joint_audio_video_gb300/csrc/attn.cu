@@ -36,11 +36,14 @@
 // Softmax works in the log2 domain with a per-row running maximum that is
 // only moved (and O, l rescaled in TMEM) when the block maximum exceeds it by
 // more than 8 (factor 256): the final O / l is exact for any such maximum.
+// The exponentials are computed against the running maximum in the same pass
+// that takes the block maximum; a block that moves it is redone.
 //
 // FP8 scores (the quantised-attention prior art that §6 of "Joint Audio-Video
 // Generation in Production" names, in the form that keeps P.V in bf16): Q and
-// K arrive as E4M3 (128 bytes per head row, one 16 KB box per tile) with a
-// per-token Q scale and a per-128-key-block K scale; S = Q8 K8^T runs as four
+// K arrive as E4M3 (128 bytes per head row: one 16 KB box per Q tile, one 8 KB
+// box of 64 keys per CTA and K block) with a per-token Q scale and a
+// per-128-key-block K scale; S = Q8 K8^T runs as four
 // kind::f8f6f4 products of K = 32, and the two scales fold into the softmax's
 // per-row, per-block constant: s = sq[i] sk[b] (q8 . k8).
 #include <cuda_bf16.h>
@@ -318,6 +321,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the even CTA lets every copy it armed land before the CTA can exit
       // (earlier pairs were consumed before their slot was refilled); the odd
       // CTA's copies count on the even CTA's barriers
+      if (!ok) abort_grace();
       if (lead) {
         WaitCtx drain{&abort_flag, p.status, kDrainWaitNs};
         volatile int no_abort = 0;

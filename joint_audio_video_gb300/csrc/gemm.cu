@@ -503,6 +503,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (++stage == S) { stage = 0; phase ^= 1u; }
         }
       }
+      if (!ok) abort_grace();
       if (!ok && lead) {
         // unwind: let the stages armed here land before the CTA exits (the
         // odd CTA's copies of a stage count on the same barrier)

@@ -84,6 +84,16 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
 // tensor memory under a running MMA.
 constexpr uint64_t kDrainWaitNs = 200000000ull;
 
+// Time a producer that gave up lets pass before its CTA can leave: in a CTA
+// pair, the copies one CTA issued count on the other CTA's barrier, so it
+// cannot observe their completion; copies in flight land within microseconds.
+constexpr uint64_t kAbortGraceNs = 100000ull;
+__device__ __forceinline__ void abort_grace() {
+  const uint64_t t0 = global_ns();
+  while (global_ns() - t0 < kAbortGraceNs) {
+  }
+}
+
 // Per-CTA context of a bounded wait.
 struct WaitCtx {
   volatile int* abort;   // shared-memory flag, raised by the first warp that gives up
