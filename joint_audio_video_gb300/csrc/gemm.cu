@@ -15,7 +15,8 @@
 // two) computes 256 x 256 tiles; see gemm_pair_kernel below.  Otherwise the
 // single-CTA form, laid out as follows (one CTA per SM, 192 threads):
 //   warp 0      TMA producer: A tile 128x64 and B tile BNx64 per k-block into a
-//               4-stage shared-memory ring (128-byte swizzle, 1 KB aligned)
+//               shared-memory ring (128-byte swizzle, 1 KB aligned; 6 stages at
+//               BN = 128, the width this form runs at)
 //   warp 1      TMEM allocation + tcgen05.mma issue (the warp runs the loop,
 //               one elected lane issues)
 //               (M=128, N=BN, K=16 per instruction) into one of two TMEM
