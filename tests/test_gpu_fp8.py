@@ -200,3 +200,44 @@ def test_block_fp8_with_segments_against_oracle(h3):
                   c.n_heads, cu_seqlens=cu)
     assert_parity(to64(out), r["out"], "fp8 block with segments: out vs exact",
                   max_rel_rms=FP8_MAX, mean_rel=FP8_MEAN, bf16_storage=False)
+
+
+@pytest.mark.parametrize("name", ["tiny", "small"])
+def test_block_fp8_scores_equal_the_quantiser(h3, name):
+    """Without segments the fp8 block's attention takes E4M3 Q and K (Q8 | K8
+    and their scales, in the block's workspace); they equal, bit for bit, what
+    h3_quantize_qk_fp8 forms from the rotated bf16 qkv the block left in its
+    workspace."""
+    c = CONFIGS[name]
+    L, d, H = c.L, c.d, c.n_heads
+    inp = block_inputs(c)
+    args = (c.n_text, c.video_t, c.video_h, c.video_w, c.audio_channels, c.audio_steps)
+    mod, pos = h3.h3_build_packed_layout(*args)
+    desc = h3.BlockDesc.make(L=L, d=d, n_heads=H)
+    nbytes = h3.h3_workspace_size_fp8(desc)
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device=DEV)
+    out = torch.empty(L, d, dtype=torch.bfloat16, device=DEV)
+    dv = {k: v.to(DEV) for k, v in inp.items() if k != "x_raw"}
+    wq, wqs, woq, wos = _quantized_weights(h3, inp["Wqkv"], inp["Wo"])
+    h3.h3_attn_block_fwd_fp8(desc, dv["x"], torch.from_numpy(mod).to(DEV),
+                             torch.from_numpy(pos).to(DEV), dv["shift"], dv["scale"], dv["gate"],
+                             wq, wqs, woq, wos, ws, nbytes, out)
+    assert h3.h3_sync_status() == 0
+    r256 = lambda n: (n + 255) // 256 * 256
+    off_qkv = r256(L * d * 2)
+    off_qk8 = off_qkv + r256(L * 3 * d * 2) + r256(L * d) + r256(L * 4)
+    off_sq = off_qk8 + r256(L * 2 * d)
+    off_sk = off_sq + r256(H * L * 4)
+    nkb = (L + 127) // 128
+    qkv = ws[off_qkv:off_qkv + L * 3 * d * 2].view(torch.bfloat16).view(L, 3 * d)
+    qk8 = ws[off_qk8:off_qk8 + L * 2 * d]
+    sq = ws[off_sq:off_sq + H * L * 4].view(torch.float32)
+    sk = ws[off_sk:off_sk + H * nkb * 4].view(torch.float32)
+    ref8 = torch.empty_like(qk8)
+    rsq = torch.empty_like(sq)
+    rsk = torch.empty_like(sk)
+    h3.h3_quantize_qk_fp8(qkv, L, H, 128, ref8, rsq, rsk)
+    assert h3.h3_sync_status() == 0
+    assert torch.equal(qk8, ref8)
+    assert torch.equal(sq.view(torch.int32), rsq.view(torch.int32))
+    assert torch.equal(sk.view(torch.int32), rsk.view(torch.int32))
