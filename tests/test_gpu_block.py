@@ -137,3 +137,22 @@ def test_block_gate_zero_returns_input(h3):
     mod, pos, _, _ = _layouts(h3, c)
     out, _, _ = _run_fused(h3, c, inp, mod, pos)
     assert torch.equal(out.cpu(), inp["x"])
+
+
+def test_block_widest_model_all_rows(h3):
+    """The widest hidden size the library takes (d = 16,384: 128 heads; 3d =
+    49,152 columns of Wqkv and of qkv) on a short ragged sequence, all rows
+    against the oracle: row strides, the CTA-pair GEMM's 256-row tiles past a
+    ragged M, and 128 attention heads."""
+    from h3inputs import BlockConfig
+    c = BlockConfig("widest", 21, 2, 5, 6, 2, 70, d=16384, n_heads=128, seed=17)
+    assert c.L == 221
+    inp = block_inputs(c)
+    mod, pos, omod, opos = _layouts(h3, c)
+    out, qkv, O = _run_fused(h3, c, inp, mod, pos)
+    o = _oracle_inputs(inp)
+    r = orc.block(o["x"], omod, opos, o["shift"], o["scale"], o["gate"], o["Wqkv"], o["Wo"],
+                  c.n_heads)
+    assert_parity(to64(qkv), r["qkv"], "widest qkv (rotated)")
+    assert_parity(to64(O), r["O"], "widest O", max_rel_rms=CHAIN_MAX_REL_RMS)
+    assert_parity(to64(out), r["out"], "widest out", bf16_storage=False)

@@ -101,7 +101,7 @@ def _check(O, qkv, H, causal, what, lse=None, exact=True):
 
 
 @pytest.mark.parametrize("L,H,causal", [(1, 1, 0), (129, 2, 0), (257, 2, 1), (1000, 2, 0),
-                                        (600, 2, 1), (4096, 4, 0)])
+                                        (600, 2, 1), (4096, 4, 0), (513, 1, 0), (1025, 2, 1)])
 def test_attention_fp8_parity(h3, L, H, causal):
     qkv = attention_qkv(L, H, seed=L + H + 7)
     ws, n = _workspace(h3, L, H)

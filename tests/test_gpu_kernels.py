@@ -140,7 +140,12 @@ def test_mrope_large_positions(h3):
 @pytest.mark.parametrize("L,H,causal", [(1, 1, 0), (5, 2, 0), (127, 1, 0), (128, 2, 0),
                                         (129, 1, 0), (255, 2, 0), (256, 1, 0), (257, 2, 0),
                                         (1000, 2, 0), (1, 1, 1), (129, 2, 1), (300, 1, 1),
-                                        (600, 2, 1)])
+                                        (600, 2, 1),
+                                        # a CTA pair covers 512 query rows: one full
+                                        # pair, one query row into the next pair (whose
+                                        # second CTA has no rows), one into its second CTA
+                                        (511, 1, 0), (512, 2, 0), (513, 1, 0), (769, 1, 0),
+                                        (1025, 2, 0), (513, 2, 1), (769, 1, 1), (1025, 1, 1)])
 def test_attention_parity(h3, L, H, causal):
     qkv = attention_qkv(L, H, seed=L + H)
     O = Guarded((L, H * 128), torch.bfloat16)

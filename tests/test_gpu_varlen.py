@@ -10,7 +10,7 @@ import torch
 
 import oracle as orc
 from h3inputs import CONFIGS, attention_qkv, block_inputs, random_rows
-from tests._parity import CHAIN_MAX_REL_RMS, assert_parity, to64
+from tests._parity import CHAIN_MAX_REL_RMS, assert_parity, assert_parity_rows, to64
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -30,13 +30,19 @@ def _run(h3, qkv, cu, H, causal):
     ([0, 10, 30], 1, 0), ([0, 10, 30, 45], 2, 0), ([0, 10, 30, 45], 1, 1),
     ([0, 7, 7, 130, 300, 301, 700], 2, 0), ([0, 7, 7, 130, 300, 301, 700], 1, 1),
     ([0, 256, 512, 1000], 1, 0), ([0, 1], 1, 0),
+    ([0, 511, 513, 1025, 1537], 2, 0), ([0, 511, 513, 1025, 1537], 1, 1),
 ])
 def test_varlen_parity(h3, cu, H, causal):
+    """Each row is held to its own RMS: a row of a one- or two-token segment
+    is of the order of |v| and carries the rounding of its bf16 weights at
+    that scale, while the rows of long segments set the slice RMS
+    (test_varlen_bound_cpu.py builds the kernel's rounding and shows the
+    slice-wide bound failing for it on the [0, 511, 513, ...] case)."""
     L = cu[-1]
     qkv = attention_qkv(L, H, seed=L + len(cu))
     O, lse = _run(h3, qkv, cu, H, causal)
     ro, rl = orc.attention_varlen(to64(qkv), cu, H, 128, causal=bool(causal))
-    assert_parity(to64(O), ro, f"varlen {cu} causal={causal}")
+    assert_parity_rows(to64(O), ro, f"varlen {cu} causal={causal}")
     np.testing.assert_allclose(to64(lse), rl, atol=2e-2, rtol=1e-3)
 
 
