@@ -61,7 +61,8 @@ def test_quantize_rows_bit_exact(h3):
     assert np.all(np.abs(qv[np.abs(to64(xb)).max(axis=1) > 0]).max(axis=1) == 448.0)
 
 
-@pytest.mark.parametrize("M,N,K", [(1, 128, 128), (300, 384, 512), (1000, 2048, 2048)])
+@pytest.mark.parametrize("M,N,K", [(1, 128, 128), (300, 384, 512), (1000, 2048, 2048),
+                                   (1, 256, 256), (257, 512, 512)])
 def test_gemm_fp8_against_oracle(h3, M, N, K):
     g = torch.Generator().manual_seed(M + N + K)
     a = torch.randn(M, K, generator=g).to(torch.bfloat16)

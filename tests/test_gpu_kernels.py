@@ -92,7 +92,10 @@ def test_adaln_bad_modality_flags_status(h3):
 
 # --------------------------------------------------------------------- projection
 @pytest.mark.parametrize("L,d", [(1, 128), (63, 256), (64, 256), (65, 256), (129, 384),
-                                 (1000, 256), (300, 2048)])
+                                 (1000, 256), (300, 2048),
+                                 # CTA-pair tiles (N % 256 == 0) with one row, and one
+                                 # row past a 256-row pair tile
+                                 (1, 256), (257, 512)])
 def test_qkv_proj_parity(h3, L, d):
     g = torch.Generator().manual_seed(L + 11 * d)
     y = torch.randn(L, d, generator=g).to(torch.bfloat16)
@@ -183,7 +186,8 @@ def test_attention_identical_keys_give_mean_of_values(h3):
 
 
 # --------------------------------------------------------------------- output projection
-@pytest.mark.parametrize("L,d", [(1, 128), (65, 256), (129, 384), (700, 2048)])
+@pytest.mark.parametrize("L,d", [(1, 128), (65, 256), (129, 384), (700, 2048), (1, 256),
+                                 (257, 512)])
 def test_out_proj_gated_residual_parity(h3, L, d):
     g = torch.Generator().manual_seed(L * 3 + d)
     O = torch.randn(L, d, generator=g).to(torch.bfloat16)
