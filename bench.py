@@ -426,6 +426,20 @@ def run_gpu(args, cfg):
         if it > 0:
             mts.append(ma.elapsed_time(mb_))
     mod_sa_ms = statistics.median(mts)
+    # yardstick: a plain device copy of x (the same bytes read and written)
+    # after the same flush
+    cts = []
+    for it in range(6):
+        flush_r.sum()
+        ma, mb_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ma.record(stream)
+        with torch.cuda.stream(stream):
+            y_sa.copy_(x)
+        mb_.record(stream)
+        torch.cuda.synchronize(dev)
+        if it > 0:
+            cts.append(ma.elapsed_time(mb_))
+    mod_copy_ms = statistics.median(cts)
     del y_sa, flush_r
 
     # ---- the MLP sub-block of the same layer (hidden 4d), timed on its own
@@ -539,7 +553,23 @@ def run_gpu(args, cfg):
     denoise_ms = statistics.median(dts)
     lat_rows = L - cfg.n_text
     denoise_bytes = lat_rows * C_lat * (4 + 2 + 4 + 4) + cfg.n_text * C_lat * 8
-    del zl, vl, x0l, flush
+    # yardstick for a launch this short: a plain device copy that moves the
+    # same number of bytes (half read, half written) after the same flush
+    src = torch.ones(denoise_bytes // 8, dtype=torch.float32, device=dev)
+    dst = torch.empty_like(src)
+    cts = []
+    for it in range(6):
+        flush.sum()
+        e_a, e_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e_a.record(stream)
+        with torch.cuda.stream(stream):
+            dst.copy_(src)
+        e_b.record(stream)
+        torch.cuda.synchronize(dev)
+        if it > 0:
+            cts.append(e_a.elapsed_time(e_b))
+    copy_same_ms = statistics.median(cts)
+    del zl, vl, x0l, flush, src, dst
 
     flops = cfg.flops()
     value = job_throughput(flops, world, ms) / 1e12
@@ -624,11 +654,15 @@ def run_gpu(args, cfg):
         "modulate_standalone": {"ms": mod_sa_ms, "bytes": 4.0 * L * d,
                                 "gbs": 4.0 * L * d / (mod_sa_ms * 1e-3) / 1e9,
                                 "frac_of_hbm_peak": 4.0 * L * d / (mod_sa_ms * 1e-3) / 1e9 / hbm,
+                                "copy_same_bytes_ms": mod_copy_ms,
+                                "frac_of_same_size_copy": mod_copy_ms / mod_sa_ms,
                                 "note": "alone, L2 flushed by a read before each call; "
                                         "modulate_hbm is the same kernel inside the step"},
         "denoise_step": {"L": L, "C": C_lat, "ms": denoise_ms,
                          "gbs": denoise_bytes / (denoise_ms * 1e-3) / 1e9,
-                         "frac_of_hbm_peak": denoise_bytes / (denoise_ms * 1e-3) / 1e9 / hbm},
+                         "frac_of_hbm_peak": denoise_bytes / (denoise_ms * 1e-3) / 1e9 / hbm,
+                         "copy_same_bytes_ms": copy_same_ms,
+                         "frac_of_same_size_copy": copy_same_ms / denoise_ms},
         "gpu_launches": 4 * args.steps,
         "clocks": clocks,
         "wall_s_timed": wall,
