@@ -26,7 +26,7 @@ from typing import Dict
 
 import torch
 
-__all__ = ["BlockConfig", "CONFIGS", "block_inputs", "sweep_modulation",
+__all__ = ["BlockConfig", "CONFIGS", "block_inputs", "block_inputs_device", "sweep_modulation",
            "attention_qkv", "random_rows"]
 
 
@@ -111,6 +111,28 @@ def block_inputs(cfg: BlockConfig, seed: int | None = None,
         "scale": scale,
         "gate": gate,
     }
+
+
+def block_inputs_device(cfg: BlockConfig, device, seed: int | None = None
+                        ) -> Dict[str, torch.Tensor]:
+    """The inputs of ``block_inputs`` (same names, shapes, dtypes and
+    distributions, drawn in the same order) from a seeded ``torch.Generator``
+    on ``device`` (torch's own Philox draw), for sequences long enough that a
+    CPU draw of x (L*d values) takes minutes.  The tensors stay on ``device``;
+    a test hands the oracle the rows it needs.  ``x_raw`` is omitted."""
+    g = torch.Generator(device=device)
+    g.manual_seed(int(cfg.seed if seed is None else seed))
+    L, d, M = cfg.L, cfg.d, cfg.n_mod
+    std_w = 1.0 / (d ** 0.5)
+
+    def draw(*shape):
+        return torch.randn(*shape, generator=g, device=device, dtype=torch.float32)
+
+    x = draw(L, d).to(torch.bfloat16)
+    wqkv = (draw(3 * d, d) * std_w).to(torch.bfloat16)
+    wo = (draw(d, d) * std_w).to(torch.bfloat16)
+    mods = {k: draw(M, d) * 0.1 for k in ("shift", "scale", "gate")}
+    return {"x": x, "Wqkv": wqkv, "Wo": wo, **mods}
 
 
 def sweep_modulation(cfg: BlockConfig, step: int) -> Dict[str, torch.Tensor]:
