@@ -8,7 +8,6 @@ protocol: keys and values for all L tokens, queries for the sampled rows).
 """
 import math
 
-import numpy as np
 import pytest
 import torch
 

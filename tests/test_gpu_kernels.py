@@ -12,7 +12,7 @@ import pytest
 import torch
 
 import oracle as orc
-from h3inputs import CONFIGS, attention_qkv, block_inputs
+from h3inputs import CONFIGS, attention_qkv
 from tests._parity import assert_parity, to64
 
 pytestmark = pytest.mark.gpu

@@ -10,7 +10,6 @@ inputs, within the block-output tolerance the other tests use.  This file is
 collected last so that a run stopping at its first failure has run every
 other test.
 """
-import numpy as np
 import pytest
 import torch
 
