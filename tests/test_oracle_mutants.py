@@ -125,10 +125,100 @@ def _layout_audio_step_major(n_text, vt, vh, vw, ac, steps):
     return mod, pos
 
 
+def _ln_eps_outside_sqrt(x, eps):
+    mu = x.mean(axis=1, keepdims=True)
+    var = ((x - mu) ** 2).mean(axis=1, keepdims=True)
+    return (x - mu) / (np.sqrt(var) + eps)
+
+
+def _modulate_shift_scale_swapped(x, mod, shift, scale, eps=1e-6):
+    return _ORIG["adaln_modulate"](x, mod, scale, shift, eps)
+
+
+def _angles_axes_swapped(pos, sections=(32, 48, 48), base=10000.0):
+    """The h and w position columns exchanged."""
+    return _ORIG["rope_angles"](np.asarray(pos)[:, [0, 2, 1]], sections, base)
+
+
+def _mrope_rotates_v(qkv, pos, n_heads, head_dim=128, sections=(32, 48, 48), base=10000.0):
+    out = _ORIG["mrope"](qkv, pos, n_heads, head_dim, sections, base)
+    L, d = qkv.shape[0], n_heads * head_dim
+    ang = core.rope_angles(pos, sections, base)
+    out[:, 2 * d:] = core.rope_rotate_heads(qkv[:, 2 * d:].reshape(L, n_heads, head_dim),
+                                            ang).reshape(L, d)
+    return out
+
+
+def _attention_v_from_k(qkv, n_heads, head_dim=128, causal=False, sm_scale=None, rows=None,
+                        k_rows_chunk=256):
+    """Values read from the K column block."""
+    d = n_heads * head_dim
+    swapped = qkv.copy()
+    swapped[:, 2 * d:] = qkv[:, d:2 * d]
+    return _ORIG["attention"](swapped, n_heads, head_dim, causal, sm_scale, rows, k_rows_chunk)
+
+
+def _attention_head_mismatch(qkv, n_heads, head_dim=128, causal=False, sm_scale=None,
+                             rows=None, k_rows_chunk=256):
+    """Head h's queries meet the keys of head h + 1."""
+    d = n_heads * head_dim
+    moved = qkv.copy()
+    moved[:, d:2 * d] = np.roll(qkv[:, d:2 * d], -head_dim, axis=1)
+    return _ORIG["attention"](moved, n_heads, head_dim, causal, sm_scale, rows, k_rows_chunk)
+
+
+def _block_residual_from_y(x, mod, pos, shift, scale, gate, wqkv, wo, n_heads, head_dim=128,
+                           causal=False, eps=1e-6, sections=(32, 48, 48), base=10000.0,
+                           cu_seqlens=None):
+    """The residual taken from the modulated y instead of the block input x."""
+    r = _ORIG["block"](x, mod, pos, shift, scale, gate, wqkv, wo, n_heads, head_dim, causal,
+                       eps, sections, base, cu_seqlens)
+    r["out"] = core.gated_residual(r["y"], r["branch"], mod, gate)
+    return r
+
+
+def _block_rows_k_unrotated(x, mod, pos, shift, scale, gate, wqkv, wo, rows, n_heads,
+                            head_dim=128, causal=False, eps=1e-6, sections=(32, 48, 48),
+                            base=10000.0):
+    """The row-slice protocol forgets to rotate the keys of the other tokens."""
+    d = n_heads * head_dim
+    rows = np.asarray(rows, dtype=np.int64)
+    y = core.adaln_modulate(x, mod, shift, scale, eps)
+    kv = core.linear(y, wqkv[d:3 * d])
+    q = core.rope_rotate_heads(core.linear(y[rows], wqkv[:d]).reshape(len(rows), n_heads,
+                                                                       head_dim),
+                               core.rope_angles(pos[rows], sections, base)).reshape(len(rows), d)
+    qkv = np.zeros((x.shape[0], 3 * d))
+    qkv[:, d:] = kv
+    qkv[rows, :d] = q
+    o, lse = core.attention(qkv, n_heads, head_dim, causal, rows=rows)
+    branch = core.linear(o, wo)
+    return {"y": y[rows], "q": q, "k": kv[:, :d], "v": kv[:, d:], "O": o, "lse": lse,
+            "branch": branch, "out": core.gated_residual(x[rows], branch, mod[rows], gate)}
+
+
+def _mlp_gelu_after_down(x, mod, shift, scale, gate, w1, w2, eps=1e-6):
+    y = core.adaln_modulate(x, mod, shift, scale, eps)
+    h = core.linear(y, w1)
+    branch = core.gelu_tanh(core.linear(h, w2))
+    return {"y": y, "h": h, "branch": branch,
+            "out": core.gated_residual(x, branch, mod, gate)}
+
+
+def _denoise_anchor_before_update(z, v_h3, mod, sigma, sigma_next, update, anchor=None,
+                                  z_anchor=None):
+    """Anchors restored before the update instead of after it."""
+    z = np.array(z, dtype=np.float64, copy=True)
+    if anchor is not None:
+        a = np.asarray(anchor).astype(bool)
+        z[a] = np.asarray(z_anchor)[a]
+    return _ORIG["denoise_step"](z, v_h3, mod, sigma, sigma_next, update, None, None)
+
+
 _ORIG = {name: getattr(core, name) for name in
          ("layer_norm", "adaln_modulate", "linear", "rope_rotate_heads",
-          "rope_angles", "attention", "attention_varlen", "gated_residual", "packed_layout",
-          "denoise_step", "gelu_tanh")}
+          "rope_angles", "mrope", "attention", "attention_varlen", "gated_residual",
+          "packed_layout", "block", "block_rows", "mlp_block", "denoise_step", "gelu_tanh")}
 
 MUTANTS = {
     "unbiased-variance": ("layer_norm", _ln_unbiased),
@@ -145,6 +235,16 @@ MUTANTS = {
     "denoise-native-velocity-sign": ("denoise_step", _denoise_native_sign),
     "denoise-shared-schedule": ("denoise_step", _denoise_shared_schedule),
     "gelu-sigmoid-form": ("gelu_tanh", _gelu_sigmoid_form),
+    "ln-eps-outside-sqrt": ("layer_norm", _ln_eps_outside_sqrt),
+    "modulate-shift-scale-swapped": ("adaln_modulate", _modulate_shift_scale_swapped),
+    "rope-h-w-positions-swapped": ("rope_angles", _angles_axes_swapped),
+    "rope-rotates-v": ("mrope", _mrope_rotates_v),
+    "attention-values-from-k-block": ("attention", _attention_v_from_k),
+    "attention-keys-of-next-head": ("attention", _attention_head_mismatch),
+    "block-residual-from-y": ("block", _block_residual_from_y),
+    "block-rows-keys-unrotated": ("block_rows", _block_rows_k_unrotated),
+    "mlp-gelu-after-down-projection": ("mlp_block", _mlp_gelu_after_down),
+    "denoise-anchor-before-update": ("denoise_step", _denoise_anchor_before_update),
 }
 
 PIN_TESTS = [getattr(pins, n) for n in dir(pins) if n.startswith("test_")]
