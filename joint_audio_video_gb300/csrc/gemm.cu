@@ -26,6 +26,8 @@
 //               so the MMA of the next tile overlaps this epilogue
 // Tiles are visited in groups of kGroupM row-tiles (all N tiles of a group
 // before the next group), so the working set of A and B stays in L2.
+#include <atomic>
+
 #include <cuda_bf16.h>
 
 #include "kernels.hpp"
@@ -654,19 +656,21 @@ cudaError_t launch_pair(const GemmArgs& a, const DevCtx& ctx, cudaStream_t st) {
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  // how many pairs can be resident at once (SM pairs of the GPU), asked once per device
-  static int resident[64];
+  // how many pairs can be resident at once (SM pairs of the GPU), asked once per
+  // device; callers on several host threads may race to fill the entry with the
+  // same value
+  static std::atomic<int> resident[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (resident[dev] <= 0) {
-    int n = 0;
-    e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+  int nres = resident[dev].load(std::memory_order_relaxed);
+  if (nres <= 0) {
+    e = cudaOccupancyMaxActiveClusters(&nres, kern, &cfg);
     if (e != cudaSuccess) return e;
-    if (n <= 0) return cudaErrorInvalidConfiguration;
-    resident[dev] = n;
+    if (nres <= 0) return cudaErrorInvalidConfiguration;
+    resident[dev].store(nres, std::memory_order_relaxed);
   }
   const int tiles = p.num_m * p.num_n;
-  const int ncl = tiles < resident[dev] ? tiles : resident[dev];
+  const int ncl = tiles < nres ? tiles : nres;
   cfg.gridDim = dim3(unsigned(2 * ncl));
   e = cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmC, p, rt);
   if (e != cudaSuccess) return e;
