@@ -231,3 +231,23 @@ def test_fp8_attention_arguments_are_validated_before_launch(lib):
     d1 = lib.BlockDesc.make(L=64, d=256, n_heads=2, cu_seqlens=[0, 20, 64])
     assert lib.h3_workspace_size_fp8(d0) - lib.h3_workspace_size_fp8(d1) == \
         lib.h3_attn_workspace_size_fp8(64, 2)
+
+
+def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
+    """No fallback: with the shared library absent, loading it and every call
+    through the binding raise instead of computing anything elsewhere."""
+    import pytest
+    import torch
+
+    import joint_audio_video_gb300 as h3
+
+    monkeypatch.setattr(h3, "_lib", None)
+    monkeypatch.setattr(h3, "lib_path", str(tmp_path / "libh3attn.so"))
+    with pytest.raises(RuntimeError, match="is missing"):
+        h3.load()
+    x = torch.zeros(4, 128, dtype=torch.bfloat16)
+    with pytest.raises(RuntimeError, match="is missing"):
+        h3.h3_adaln_modulate(x, torch.zeros(4, dtype=torch.uint8), torch.zeros(1, 128),
+                             torch.zeros(1, 128), 4, 128, 1, 1e-6, torch.empty_like(x))
+    with pytest.raises(RuntimeError, match="is missing"):
+        h3.h3_build_packed_layout(1, 1, 1, 1, 1, 1)
