@@ -40,13 +40,17 @@ def _workload(cfg) -> str:
             f"full attention, batch 1")
 
 
+L2_BYTES = 129e6   # GB300 L2
+
+
 def _config(cfg, world: int = 1) -> dict:
     """The workload description both arms print (same keys, same values)."""
+    x_b, qkv_b = cfg.L * cfg.d * 2, cfg.L * 3 * cfg.d * 2
+    sizes = f"x {x_b / 1e6:.0f} MB, qkv {qkv_b / 1e9:.2f} GB per step"
+    l2 = (f"inputs larger than L2 ({sizes})" if x_b + qkv_b > L2_BYTES else
+          f"working set fits in the 129 MB L2 ({sizes}): steps run L2-warm, no flush")
     return {"workload": _workload(cfg), "L": cfg.L, "d": cfg.d, "heads": cfg.n_heads,
-            "causal": False,
-            "l2": f"inputs larger than L2 (x {cfg.L * cfg.d * 2 / 1e6:.0f} MB, qkv "
-                  f"{cfg.L * 3 * cfg.d * 2 / 1e9:.2f} GB per step)",
-            "parallelism": f"replicas x{world}"}
+            "causal": False, "l2": l2, "parallelism": f"replicas x{world}"}
 
 
 def _peaks():
