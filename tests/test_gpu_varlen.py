@@ -79,15 +79,21 @@ def test_one_segment_equals_full_attention_bitwise(h3):
     assert torch.equal(a, b)
 
 
-def test_varlen_full_size_modality_segments(h3):
+@pytest.mark.parametrize("causal", [0, 1])
+def test_varlen_full_size_modality_segments(h3, causal):
     c = CONFIGS["full"]
     cu = [0, c.n_text, c.n_text + c.n_video, c.L]
     qkv = attention_qkv(c.L, c.n_heads, seed=61)
-    O, _ = _run(h3, qkv, cu, c.n_heads, 0)
+    O, _ = _run(h3, qkv, cu, c.n_heads, causal)
     rows = np.unique(np.concatenate([random_rows(c.L, 40, seed=8).numpy(),
                                      np.array([0, 357, 358, 359, 57957, 57958, c.L - 1])]))
-    ro, _ = orc.attention_varlen(to64(qkv), cu, c.n_heads, 128, rows=rows)
+    ro, _ = orc.attention_varlen(to64(qkv), cu, c.n_heads, 128, causal=bool(causal), rows=rows)
     got = to64(O[torch.from_numpy(rows).to(DEV)])
+    if causal:
+        # a causal row of a segment sees the keys from the segment start to
+        # itself (1 to 57,600): each row against its own RMS, as for causal rows
+        assert_parity_rows(got, ro, "full-size modality segments, causal")
+        return
     # segments are independent attention problems with very different output
     # scales (358 text keys vs 57,600 video keys): each is held to its own RMS
     seg = np.searchsorted(np.array(cu), rows, side="right") - 1
