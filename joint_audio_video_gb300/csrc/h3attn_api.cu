@@ -66,6 +66,9 @@ bool overlap(const void* a, size_t na, const void* b, size_t nb) {
 }
 
 bool valid_d(int32_t d) { return d >= 128 && d <= 16384 && d % 128 == 0; }
+// head counts of 128-wide heads that give a valid d (checked before any
+// multiplication, so a huge count cannot wrap around to a valid width)
+bool valid_heads(int32_t n_heads) { return n_heads >= 1 && n_heads <= 16384 / 128; }
 
 h3_status launched(cudaError_t e) { return e == cudaSuccess ? H3_OK : H3_ERR_CUDA; }
 
@@ -232,7 +235,7 @@ h3_status h3_mrope_apply(uint16_t* qkv, const int32_t* pos, int32_t L, int32_t n
   const Trace trace_("h3_mrope_apply");
   if (L < 1 || n_heads < 1) return H3_ERR_INVALID_ARG;
   if (head_dim != 128) return H3_ERR_UNSUPPORTED;
-  if (!valid_d(n_heads * 128)) return H3_ERR_INVALID_ARG;
+  if (!valid_heads(n_heads)) return H3_ERR_INVALID_ARG;
   if (h3_status s = check_rope(sec, head_dim, base)) return s;
   if (!aligned16(qkv) || pos == nullptr || (reinterpret_cast<uintptr_t>(pos) & 3u))
     return H3_ERR_INVALID_ARG;
@@ -251,7 +254,7 @@ h3_status h3_joint_attn_fwd(const uint16_t* qkv, int32_t L, int32_t n_heads, int
   const Trace trace_("h3_joint_attn_fwd");
   if (L < 1 || n_heads < 1) return H3_ERR_INVALID_ARG;
   if (head_dim != 128) return H3_ERR_UNSUPPORTED;
-  if (!valid_d(n_heads * 128)) return H3_ERR_INVALID_ARG;
+  if (!valid_heads(n_heads)) return H3_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return H3_ERR_INVALID_ARG;
   if (!(sm_scale > 0.f) || !std::isfinite(sm_scale)) return H3_ERR_INVALID_ARG;
   if (!aligned16(qkv) || !aligned16(O)) return H3_ERR_INVALID_ARG;
@@ -279,7 +282,7 @@ h3_status h3_joint_attn_varlen_fwd(const uint16_t* qkv, const int32_t* cu_seqlen
   const Trace trace_("h3_joint_attn_varlen_fwd");
   if (L < 1 || n_heads < 1) return H3_ERR_INVALID_ARG;
   if (head_dim != 128) return H3_ERR_UNSUPPORTED;
-  if (!valid_d(n_heads * 128)) return H3_ERR_INVALID_ARG;
+  if (!valid_heads(n_heads)) return H3_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return H3_ERR_INVALID_ARG;
   if (!(sm_scale > 0.f) || !std::isfinite(sm_scale)) return H3_ERR_INVALID_ARG;
   if (h3_status s = check_segments(cu_seqlens, n_seg, L)) return s;
@@ -313,7 +316,7 @@ h3_status h3_attn_workspace_size_fp8(int32_t L, int32_t n_heads, int32_t head_di
                                      size_t* bytes) {
   if (bytes == nullptr || L < 1 || n_heads < 1) return H3_ERR_INVALID_ARG;
   if (head_dim != 128) return H3_ERR_UNSUPPORTED;
-  if (!valid_d(n_heads * 128)) return H3_ERR_INVALID_ARG;
+  if (!valid_heads(n_heads)) return H3_ERR_INVALID_ARG;
   *bytes = attn_fp8_bytes(size_t(L), size_t(n_heads));
   return H3_OK;
 }
@@ -323,7 +326,7 @@ h3_status h3_quantize_qk_fp8(const uint16_t* qkv, int32_t L, int32_t n_heads, in
   const Trace trace_("h3_quantize_qk_fp8");
   if (L < 1 || n_heads < 1) return H3_ERR_INVALID_ARG;
   if (head_dim != 128) return H3_ERR_UNSUPPORTED;
-  if (!valid_d(n_heads * 128)) return H3_ERR_INVALID_ARG;
+  if (!valid_heads(n_heads)) return H3_ERR_INVALID_ARG;
   if (!aligned16(qkv) || !aligned16(qk8) || sq == nullptr || sk == nullptr ||
       (reinterpret_cast<uintptr_t>(sq) & 3u) || (reinterpret_cast<uintptr_t>(sk) & 3u))
     return H3_ERR_INVALID_ARG;
@@ -346,7 +349,7 @@ h3_status h3_joint_attn_fwd_fp8(const uint16_t* qkv, int32_t L, int32_t n_heads,
   const Trace trace_("h3_joint_attn_fwd_fp8");
   if (L < 1 || n_heads < 1) return H3_ERR_INVALID_ARG;
   if (head_dim != 128) return H3_ERR_UNSUPPORTED;
-  if (!valid_d(n_heads * 128)) return H3_ERR_INVALID_ARG;
+  if (!valid_heads(n_heads)) return H3_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return H3_ERR_INVALID_ARG;
   if (!(sm_scale > 0.f) || !std::isfinite(sm_scale)) return H3_ERR_INVALID_ARG;
   if (!aligned16(qkv) || !aligned16(O) || workspace == nullptr ||
@@ -526,6 +529,8 @@ h3_status h3_gemm_fp8(const uint8_t* A, const float* a_scale, const uint8_t* B,
                       h3_stream_t stream) {
   const Trace trace_("h3_gemm_fp8");
   if (M < 1 || N < 128 || N % 128 != 0 || K < 128 || K % 128 != 0) return H3_ERR_INVALID_ARG;
+  // the kernels count output tiles (at least 128 x 128) in 32-bit integers
+  if ((int64_t(M) + 127) / 128 * (int64_t(N) / 128) > INT32_MAX) return H3_ERR_INVALID_ARG;
   if (!aligned16(A) || !aligned16(B) || !aligned16(C) || !aligned16(a_scale) ||
       !aligned16(b_scale))
     return H3_ERR_INVALID_ARG;
@@ -724,7 +729,9 @@ static h3_status check_desc(const h3_block_desc* desc) {
   if (desc->L < 1 || desc->n_heads < 1 || desc->n_mod < 1 || desc->n_mod > 255)
     return H3_ERR_INVALID_ARG;
   if (desc->head_dim != 128) return H3_ERR_UNSUPPORTED;
-  if (desc->d != desc->n_heads * desc->head_dim || !valid_d(desc->d)) return H3_ERR_INVALID_ARG;
+  if (!valid_heads(desc->n_heads) || desc->d != desc->n_heads * desc->head_dim ||
+      !valid_d(desc->d))
+    return H3_ERR_INVALID_ARG;
   if (desc->causal != 0 && desc->causal != 1) return H3_ERR_INVALID_ARG;
   if (!(desc->ln_eps >= 0.f) || !std::isfinite(desc->ln_eps)) return H3_ERR_INVALID_ARG;
   if (desc->n_seg != 0) {

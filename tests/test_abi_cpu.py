@@ -251,3 +251,28 @@ def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
                              torch.zeros(1, 128), 4, 128, 1, 1e-6, torch.empty_like(x))
     with pytest.raises(RuntimeError, match="is missing"):
         h3.h3_build_packed_layout(1, 1, 1, 1, 1, 1)
+
+
+def test_extreme_counts_cannot_wrap_into_valid_sizes(lib):
+    """A head count whose width n_heads * 128 wraps around 32 bits to a valid d,
+    or an fp8 GEMM whose tile count would not fit 32 bits, is rejected before
+    any launch."""
+    L = lib.load()
+    p = 1 << 20
+    INV = 1
+    wrap = (1 << 25) + 1            # (2^25 + 1) * 128 = 2^32 + 128 -> 128 in 32 bits
+    sec = (ctypes.c_int32 * 3)(32, 48, 48)
+    far = p + (1 << 30)
+    assert L.h3_joint_attn_fwd(p, 8, wrap, 128, 0, 0.1, far, None, None) == INV
+    assert L.h3_joint_attn_fwd(p, 8, 129, 128, 0, 0.1, far, None, None) == INV
+    assert L.h3_mrope_apply(p, p, 8, wrap, 128, ctypes.addressof(sec), 1e4, None) == INV
+    cu = (ctypes.c_int32 * 2)(0, 8)
+    assert L.h3_joint_attn_varlen_fwd(p, ctypes.addressof(cu), 1, 8, wrap, 128, 0, 0.1, far,
+                                      None, None) == INV
+    desc = lib.BlockDesc.make(L=64, d=256, n_heads=2)
+    desc.n_heads = wrap
+    desc.d = 128                    # = wrap * 128 in 32 bits
+    nbytes = ctypes.c_size_t(0)
+    assert L.h3_workspace_size(ctypes.byref(desc), ctypes.byref(nbytes)) == INV
+    big = (1 << 31) - 128
+    assert L.h3_gemm_fp8(p, p, p, p, big, big, 128, far, None) == INV
