@@ -16,7 +16,11 @@ extern "C" h3_status h3_build_packed_layout(int32_t n_text, int32_t video_t, int
   if (n_text < 0 || video_t < 0 || video_h < 0 || video_w < 0 || audio_channels < 0 ||
       audio_steps < 0 || mod == nullptr || pos == nullptr)
     return H3_ERR_INVALID_ARG;
-  const int64_t n_video = int64_t(video_t) * video_h * video_w;
+  // h * w first (< 2^62); a frame larger than any valid L is rejected before
+  // the product with t could leave 64 bits
+  const int64_t n_frame = int64_t(video_h) * video_w;
+  if (video_t > 0 && n_frame > INT32_MAX) return H3_ERR_INVALID_ARG;
+  const int64_t n_video = int64_t(video_t) * n_frame;
   const int64_t n_audio = int64_t(audio_channels) * audio_steps;
   const int64_t L = int64_t(n_text) + n_video + n_audio;
   if (L < 1 || L > capacity || L > INT32_MAX) return H3_ERR_INVALID_ARG;

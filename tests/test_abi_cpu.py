@@ -276,3 +276,13 @@ def test_extreme_counts_cannot_wrap_into_valid_sizes(lib):
     assert L.h3_workspace_size(ctypes.byref(desc), ctypes.byref(nbytes)) == INV
     big = (1 << 31) - 128
     assert L.h3_gemm_fp8(p, p, p, p, big, big, 128, far, None) == INV
+
+
+def test_layout_counts_too_large_for_64_bits_are_rejected(lib):
+    L = lib.load()
+    big = (1 << 31) - 1
+    mod = (ctypes.c_uint8 * 4)()
+    pos = (ctypes.c_int32 * 12)()
+    assert L.h3_build_packed_layout(0, big, big, big, 0, 0, mod, pos, 4) == 1
+    assert L.h3_build_packed_layout(0, 0, 0, 0, big, big, mod, pos, 4) == 1
+    assert L.h3_build_packed_layout(big, 1, 1, 1, 0, 0, mod, pos, 4) == 1
